@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused, chunked top-K KL loss (forward + backward) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload longctx]
+    python bench.py --impl reference ...      # the fp64 CPU oracle, timed on host cores
+
+One step = one ``kd_topk_kl_fused_step`` over the whole workload: every chunk's
+prep, logits GEMM with fused softmax partials and top-K gather, combine,
+logits GEMM again with the gradient epilogue, dH = G W and dW += G^T H.
+Default workload: the long-context head (T 32768, d 3072, V 128256, K 100,
+chunk 2048).  Inputs are seeded synthetic tensors of that shape; W alone
+(788 MB) is larger than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``value`` is tokens/s of the whole job with
+inputs resident in HBM; ``e2e`` repeats the measurement through the public
+API with the step's inputs (H, idx, p) copied from pinned host memory and the
+loss read back every step.  N > 1 runs one independent replica per GPU
+(torchrun; the path needs no data exchange for this metric), timed between
+barriers, max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); peak bytes vs T"
+
+# DRAM traffic of the dominant kernel from an ncu capture (see profiles/);
+# reported only while the kernel sources still hash to what was captured.
+TRAFFIC = {"kernel": None, "bytes_per_launch": None, "src_sha": None}
+KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300/csrc/kd_ptx.cuh",
+                  "lm_head_top_tma_b300/csrc/kdtopk.cu"]
+
+
+def kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16": float(pk["bf16_tflops"]), "bf16_sustained": float(pk["bf16_tflops_sustained"]),
+                "hbm": float(pk["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16": 1800.0, "bf16_sustained": 1400.0, "hbm": 6400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="kd_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path).read().splitlines():
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ dist
+def dist_setup(n_gpus: int):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=ws)
+    return rank, local, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_tokens_per_s(H_cpu, W_cpu, idx, p, target_s: float, rows0: int = 32):
+    """Time the fp64 oracle (forward + backward incl. dW) on a bounded row sample."""
+    import numpy as np
+    from oracle import kd_oracle
+
+    Wd = W_cpu.double().numpy()
+    T = H_cpu.shape[0]
+    n = min(rows0, T)
+    t0 = time.perf_counter()
+    kd_oracle(H_cpu[:n], Wd, idx[:n], p[:n])
+    dt = time.perf_counter() - t0
+    rows = int(min(T, max(n, n * target_s / max(dt, 1e-6))))
+    rows = max(n, (rows // 32) * 32)
+    t0 = time.perf_counter()
+    kd_oracle(H_cpu[:rows], Wd, idx[:rows], p[:rows])
+    dt = time.perf_counter() - t0
+    cores = _blas_threads()
+    return rows / dt, rows, dt, cores
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    from lm_head_top_tma_b300.inputs import get_workload, make_cache, make_hw
+    from oracle import kd_oracle
+
+    wl = get_workload(args.workload)
+    per_step_s = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = 32
+    H, W = make_hw(wl.T, wl.d, wl.V, wl.kind, wl.seed, device="cpu")
+    idx, p = make_cache(wl.T, wl.V, wl.K, wl.kind, wl.seed)
+    Wd = W.double().numpy()
+    t0 = time.perf_counter()
+    kd_oracle(H[:rows], Wd, idx[:rows], p[:rows])
+    dt = time.perf_counter() - t0
+    rows = int(max(32, min(wl.T, rows * per_step_s / max(dt, 1e-6))) // 32 * 32)
+    times = []
+    for s in range(args.warmup + args.steps):
+        r0 = (s * rows) % max(1, wl.T - rows + 1)
+        t0 = time.perf_counter()
+        kd_oracle(H[r0:r0 + rows], Wd, idx[r0:r0 + rows], p[r0:r0 + rows])
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = rows * len(times) / tot
+    cores = _blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} token rows per step of the {wl.name} workload, fp64 forward+backward "
+                                   f"(z, lse, loss, G, dH, dW) with the full W[{wl.V},{wl.d}]"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(wl):
+    return {"workload": wl.name, "T": wl.T, "d": wl.d, "V": wl.V, "K": wl.K, "chunk": wl.chunk,
+            "seed": wl.seed, "l2": "inputs larger than L2 (W alone is %.0f MB), no flush" % (wl.V * wl.d * 2 / 1e6)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_kdtopk(args):
+    import numpy as np
+    import torch
+
+    from lm_head_top_tma_b300 import api
+    from lm_head_top_tma_b300.inputs import get_workload, make_inputs
+
+    rank, local, ws = dist_setup(args.gpus)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    wl = get_workload(args.workload)
+    inp = make_inputs(wl, device=dev, seed=wl.seed + rank)
+    H, W = inp["H"], inp["W"]
+    idx = torch.as_tensor(inp["idx"]).to(dev)
+    p = torch.as_tensor(inp["p"]).to(dev)
+    T, d, V, K, C = wl.T, wl.d, wl.V, wl.K, wl.chunk
+    torch.cuda.reset_peak_memory_stats(dev)
+    work = api.Workspace(dev)
+    out = {"loss": torch.empty(1, device=dev), "lse": torch.empty(T, device=dev),
+           "dH": torch.empty(T, d, device=dev), "dW": torch.empty(V, d, device=dev)}
+    stream = torch.cuda.current_stream(dev)
+
+    def step(h=H, i=idx, pp=p):
+        api.fused_step(h, W, i, pp, C, workspace=work, out=out, check=False)
+
+    for _ in range(args.warmup):
+        step()
+    from lm_head_top_tma_b300 import _native as N
+
+    N.check(api.device_status(work.buf, dev), "warm-up")
+    torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region
+    api.profile_enable(True)
+    api.profile_read(reset=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    prof = api.profile_read(reset=True)
+    api.profile_enable(False)
+    N.check(api.device_status(work.buf, dev), "timed steps")
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms, ws)
+    tokens_per_s = ws * T / (ms / 1e3)
+
+    # ---- end to end: host inputs copied in, loss read back, every step
+    Hh = H.cpu().pin_memory()
+    ih = idx.cpu().pin_memory()
+    ph = p.cpu().pin_memory()
+    Hd, idd, pd = torch.empty_like(H), torch.empty_like(idx), torch.empty_like(p)
+    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        Hd.copy_(Hh, non_blocking=True)
+        idd.copy_(ih, non_blocking=True)
+        pd.copy_(ph, non_blocking=True)
+        step(Hd, idd, pd)
+        loss_h.copy_(out["loss"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws)
+    h2d = Hh.numel() * Hh.element_size() + ih.numel() * 4 + ph.numel() * 4
+    peak_bytes = torch.cuda.max_memory_allocated(dev)
+
+    nchunks = math.ceil(T / C)
+    flops_8 = 8.0 * T * V * d
+    flops_6 = 6.0 * T * V * d
+    peaks = load_peaks()
+    # dominant kernel: the kind with the largest total time inside the timed region
+    gemm_kinds = ("logits_fwd", "logits_g", "gemm_dh", "gemm_dw")
+    dom = max(prof, key=lambda k: prof[k][0])
+    dom_ms, dom_n = prof[dom]
+    per_launch_flops = 2.0 * min(C, T) * V * d if dom in gemm_kinds else None
+    achieved = per_launch_flops / (dom_ms / dom_n / 1e3) / 1e12 if per_launch_flops and dom_n else None
+    traffic = TRAFFIC["bytes_per_launch"] if (TRAFFIC["kernel"] == dom and
+                                              TRAFFIC["src_sha"] == kernel_src_sha()) else None
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": (achieved / peaks["bf16_sustained"]) if achieved else None,
+                "traffic": traffic, "peak_kind": f"bf16 sustained ({peaks['source']})",
+                "frac_of_burst_peak": (achieved / peaks["bf16"]) if achieved else None,
+                "per_kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
+                "launches_per_step": {k: v[1] // args.steps for k, v in prof.items() if v[1]}}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        Hc = H[: min(T, 4096)].cpu()
+        v, rows, dt, cores = oracle_tokens_per_s(Hc, W.cpu(), inp["idx"], inp["p"], args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {rows} token rows of the {wl.name} workload, fp64 forward+backward "
+                         f"with the full W[{V},{d}] ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(wl),
+            "tflops_8TVd": ws * flops_8 / (ms / 1e3) / 1e12,
+            "tflops_6TVd": ws * flops_6 / (ms / 1e3) / 1e12,
+            "frac_of_bf16_peak": {"burst": ws * flops_8 / (ms / 1e3) / 1e12 / ws / peaks["bf16"],
+                                  "sustained": ws * flops_8 / (ms / 1e3) / 1e12 / ws / peaks["bf16_sustained"],
+                                  "source": peaks["source"]},
+            "workspace_bytes": work.nbytes, "peak_bytes": peak_bytes,
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": 4},
+            "gpu_launches": 8 * nchunks * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kdtopk", choices=["kdtopk", "reference"])
+    ap.add_argument("--workload", default="longctx")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_kdtopk(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

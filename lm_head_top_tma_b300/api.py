@@ -1,0 +1,207 @@
+"""Torch-facing binding of the C ABI: argument checks and marshalling only.
+
+Every step of the loss runs in the CUDA kernels of libkdtopk.so; torch only
+provides device memory (inputs, outputs, workspace) and the current stream.
+Names follow the C entry points: ``forward``, ``backward``, ``fused_step``.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native as N
+
+__all__ = ["workspace_size", "Workspace", "forward", "backward", "fused_step",
+           "device_status", "gemm_bf16", "debug_wait_timeout", "TopKKLLoss",
+           "profile_enable", "profile_read"]
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype, ndim, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _what(kind) -> int:
+    return {"forward": N.KD_WS_FORWARD, "backward": N.KD_WS_BACKWARD,
+            "fused": N.KD_WS_FUSED}[kind]
+
+
+def workspace_size(T: int, d: int, V: int, K: int, chunk: int, what: str = "fused") -> int:
+    n = N.load().kd_topk_kl_workspace_size(int(T), int(d), int(V), int(K), int(chunk), _what(what))
+    if n == 0:
+        raise ValueError(f"unsupported sizes T={T} d={d} V={V} K={K} chunk={chunk}")
+    return int(n)
+
+
+class Workspace:
+    """Device scratch for the chunk loop, grown on demand and reused."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(int(nbytes), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+    @property
+    def nbytes(self) -> int:
+        return 0 if self.buf is None else self.buf.numel()
+
+
+def _inputs(H, W, idx, p):
+    _need(H, "H", torch.bfloat16, 2)
+    dev = H.device
+    _need(W, "W", torch.bfloat16, 2, dev)
+    _need(idx, "idx", torch.int32, 2, dev)
+    _need(p, "p", torch.float32, 2, dev)
+    T, d = H.shape
+    V, d2 = W.shape
+    if d2 != d:
+        raise ValueError("H and W disagree on d")
+    if idx.shape != p.shape or idx.shape[0] != T:
+        raise ValueError("idx and p must both be [T, K]")
+    return dev, T, d, V, idx.shape[1]
+
+
+def device_status(ws: torch.Tensor, device=None) -> int:
+    return N.load().kd_topk_kl_device_status(_ptr(ws), _stream(device or ws.device))
+
+
+def _finish(ws, dev, where, check):
+    if check:
+        N.check(device_status(ws, dev), where)
+
+
+def forward(H, W, idx, p, chunk: int, *, loss_rows: bool = False, workspace: Workspace | None = None,
+            check: bool = True):
+    """Loss (1-element fp32 tensor), lse [T] and optionally per-row losses [T]."""
+    dev, T, d, V, K = _inputs(H, W, idx, p)
+    ws_n = workspace_size(T, d, V, K, chunk, "forward")
+    ws = (workspace or Workspace(dev)).get(ws_n)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    lrows = torch.empty(T, dtype=torch.float32, device=dev) if loss_rows else None
+    rc = N.load().kd_topk_kl_forward(_ptr(H), _ptr(W), _ptr(idx), _ptr(p), T, d, V, K, int(chunk),
+                                     _ptr(loss), _ptr(lse), _ptr(lrows), _ptr(ws), ws.numel(), _stream(dev))
+    N.check(rc, "kd_topk_kl_forward")
+    _finish(ws, dev, "kd_topk_kl_forward", check)
+    return (loss, lse, lrows) if loss_rows else (loss, lse)
+
+
+def backward(H, W, idx, p, lse, chunk: int, *, dloss: float = 1.0, dW: torch.Tensor | None = None,
+             accumulate_dW: bool = False, workspace: Workspace | None = None, check: bool = True):
+    """dH [T,d] fp32 and dW [V,d] fp32 (``dW`` is overwritten, or added to)."""
+    dev, T, d, V, K = _inputs(H, W, idx, p)
+    _need(lse, "lse", torch.float32, 1, dev)
+    ws_n = workspace_size(T, d, V, K, chunk, "backward")
+    ws = (workspace or Workspace(dev)).get(ws_n)
+    dH = torch.empty(T, d, dtype=torch.float32, device=dev)
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs a dW tensor")
+        dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    _need(dW, "dW", torch.float32, 2, dev)
+    rc = N.load().kd_topk_kl_backward(_ptr(H), _ptr(W), _ptr(idx), _ptr(p), _ptr(lse), T, d, V, K, int(chunk),
+                                      float(dloss), _ptr(dH), _ptr(dW), int(bool(accumulate_dW)),
+                                      _ptr(ws), ws.numel(), _stream(dev))
+    N.check(rc, "kd_topk_kl_backward")
+    _finish(ws, dev, "kd_topk_kl_backward", check)
+    return dH, dW
+
+
+def fused_step(H, W, idx, p, chunk: int, *, dloss: float = 1.0, dW: torch.Tensor | None = None,
+               accumulate_dW: bool = False, loss_rows: bool = False, workspace: Workspace | None = None,
+               check: bool = True, out: dict | None = None):
+    """Forward + backward in one chunk loop.  Returns a dict with loss, lse,
+    dH, dW (and loss_rows).  ``out`` may supply preallocated outputs."""
+    dev, T, d, V, K = _inputs(H, W, idx, p)
+    ws_n = workspace_size(T, d, V, K, chunk, "fused")
+    ws = (workspace or Workspace(dev)).get(ws_n)
+    o = out if out is not None else {}
+    loss = o.get("loss") if o.get("loss") is not None else torch.empty(1, dtype=torch.float32, device=dev)
+    lse = o.get("lse") if o.get("lse") is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    dH = o.get("dH") if o.get("dH") is not None else torch.empty(T, d, dtype=torch.float32, device=dev)
+    if dW is None:
+        dW = o.get("dW") if o.get("dW") is not None else torch.empty(V, d, dtype=torch.float32, device=dev)
+    lrows = None
+    if loss_rows:
+        lrows = o.get("loss_rows") if o.get("loss_rows") is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    rc = N.load().kd_topk_kl_fused_step(_ptr(H), _ptr(W), _ptr(idx), _ptr(p), T, d, V, K, int(chunk),
+                                        float(dloss), _ptr(loss), _ptr(lse), _ptr(lrows), _ptr(dH), _ptr(dW),
+                                        int(bool(accumulate_dW)), _ptr(ws), ws.numel(), _stream(dev))
+    N.check(rc, "kd_topk_kl_fused_step")
+    _finish(ws, dev, "kd_topk_kl_fused_step", check)
+    res = {"loss": loss, "lse": lse, "dH": dH, "dW": dW}
+    if loss_rows:
+        res["loss_rows"] = lrows
+    return res
+
+
+def gemm_bf16(A, B, M, N_, K, *, a_mn=False, b_mn=False, out=None, check=True):
+    """D = A B^T on the library's tcgen05 GEMM (A [M,K] or [K,M]; B [N,K] or [K,N])."""
+    dev = A.device
+    D = out if out is not None else torch.empty(M, N_, dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    rc = N.load().kd_gemm_bf16(_ptr(A), _ptr(B), _ptr(D), M, N_, K, A.stride(0), B.stride(0), D.stride(0),
+                               int(a_mn), int(b_mn), _ptr(ws), ws.numel(), _stream(dev))
+    N.check(rc, "kd_gemm_bf16")
+    _finish(ws, dev, "kd_gemm_bf16", check)
+    return D
+
+
+def debug_wait_timeout(limit_ms: int, device=None) -> int:
+    dev = torch.device(device or "cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    return N.load().kd_debug_wait_timeout(int(limit_ms), _ptr(ws), ws.numel(), _stream(dev))
+
+
+def profile_enable(on: bool = True):
+    N.check(N.load().kd_profile_enable(int(bool(on))), "kd_profile_enable")
+
+
+def profile_read(reset: bool = True) -> dict:
+    lib = N.load()
+    ms = (ctypes.c_double * N.KD_PROF_KINDS)()
+    cnt = (ctypes.c_int64 * N.KD_PROF_KINDS)()
+    lib.kd_profile_read(ms, cnt, N.KD_PROF_KINDS, int(bool(reset)))
+    return {lib.kd_profile_kind_name(k).decode(): (float(ms[k]), int(cnt[k]))
+            for k in range(N.KD_PROF_KINDS)}
+
+
+class TopKKLLoss(torch.autograd.Function):
+    """Autograd wrapper: loss = kd_topk_kl_forward(H, W, idx, p); the backward
+    calls kd_topk_kl_backward with the incoming gradient as dloss."""
+
+    @staticmethod
+    def forward(ctx, H, W, idx, p, chunk):
+        loss, lse = forward(H, W, idx, p, chunk)
+        ctx.save_for_backward(H, W, idx, p, lse)
+        ctx.chunk = chunk
+        return loss[0]
+
+    @staticmethod
+    def backward(ctx, g):
+        H, W, idx, p, lse = ctx.saved_tensors
+        dH, dW = backward(H, W, idx, p, lse, ctx.chunk, dloss=float(g))
+        return dH.to(H.dtype), dW.to(W.dtype), None, None, None

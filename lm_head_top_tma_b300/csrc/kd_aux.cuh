@@ -1,0 +1,185 @@
+// SIMT kernels around the tensor-core GEMMs of the chunk loop:
+//   prep     teacher-cache rows -> ids sorted ascending (with their p), the
+//            teacher mass M_t = sum_k p_tk and E_t = sum_k p_tk log p_tk,
+//            plus the id range check;
+//   combine  per-(row, vocabulary tile) softmax partials -> lse_t and the
+//            per-row loss L_t = E_t - sum_k p_tk z_tk + M_t lse_t;
+//   reductions of the loss (fp64, fixed order) and of split-K dH partials.
+#pragma once
+
+#include <math.h>
+#include <stdint.h>
+
+#include "kd_ptx.cuh"
+#include "kdtopk.h"
+
+namespace kd {
+
+constexpr int PREP_WARPS = 4;
+
+// One warp per chunk row; a bitonic network over Kpad (power of two >= K)
+// slots in shared memory, padded with INT_MAX ids.
+__global__ void __launch_bounds__(PREP_WARPS * 32)
+    kd_prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ p, int rows_valid,
+                   int Cpad, int K, int Kpad, int V, int32_t* __restrict__ sidx, float* __restrict__ sp,
+                   float* __restrict__ rowM, float* __restrict__ rowE, int* status) {
+  extern __shared__ uint8_t sm_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * PREP_WARPS + warp;
+  if (r >= Cpad) return;
+  int32_t* key = reinterpret_cast<int32_t*>(sm_raw) + warp * 2 * Kpad;
+  float* val = reinterpret_cast<float*>(key + Kpad);
+  const bool live = r < rows_valid;
+  bool bad = false;
+  for (int k = lane; k < Kpad; k += 32) {
+    int id = INT_MAX;
+    float pv = 0.f;
+    if (live && k < K) {
+      id = __ldg(idx + static_cast<size_t>(r) * K + k);
+      pv = __ldg(p + static_cast<size_t>(r) * K + k);
+      if (id < 0 || id >= V) bad = true;
+    }
+    key[k] = id;
+    val[k] = pv;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  __syncwarp();
+  for (int size = 2; size <= Kpad; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = lane; i < Kpad; i += 32) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;
+          const int a = key[i], b = key[j];
+          if ((a > b) == up) {
+            key[i] = b;
+            key[j] = a;
+            const float t = val[i];
+            val[i] = val[j];
+            val[j] = t;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+  float m = 0.f, e = 0.f;
+  for (int k = lane; k < K; k += 32) {
+    const float pv = val[k];
+    m += pv;
+    if (pv > 0.f) e += pv * logf(pv);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m += __shfl_xor_sync(0xffffffffu, m, o);
+    e += __shfl_xor_sync(0xffffffffu, e, o);
+  }
+  if (bad) {  // the row contributes nothing; the caller learns it from the status word
+    m = 0.f;
+    e = 0.f;
+  }
+  for (int k = lane; k < K; k += 32) {
+    sidx[static_cast<size_t>(r) * K + k] = bad ? INT_MAX : key[k];
+    sp[static_cast<size_t>(r) * K + k] = bad ? 0.f : val[k];
+  }
+  if (lane == 0) {
+    rowM[r] = m;
+    rowE[r] = e;
+    if (bad) atomicCAS(status, 0, KD_ERR_BAD_INDEX);
+  }
+}
+
+constexpr int COMBINE_WARPS = 8;
+
+// Block = 32 rows x 8 warps; warp w folds vocabulary tiles w, w+8, ...
+__global__ void __launch_bounds__(COMBINE_WARPS * 32)
+    kd_combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+                      const float* __restrict__ ppz, int nt, int ld_part, int rows_valid,
+                      const float* __restrict__ rowM, const float* __restrict__ rowE,
+                      float* __restrict__ lse_out, float* __restrict__ loss_rows_out,
+                      double* __restrict__ Lrow) {
+  __shared__ float s_m[COMBINE_WARPS][32], s_s[COMBINE_WARPS][32], s_z[COMBINE_WARPS][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 32 + lane;
+  float m = -INFINITY, s = 0.f, z = 0.f;
+  if (r < rows_valid) {
+    for (int t = warp; t < nt; t += COMBINE_WARPS) {
+      const size_t o = static_cast<size_t>(t) * ld_part + r;
+      const float a = pm[o], b = ps[o];
+      z += ppz[o];
+      if (a > m) {
+        s = s * ex2(m - a) + b;
+        m = a;
+      } else if (a > -INFINITY) {
+        s += b * ex2(a - m);
+      }
+    }
+  }
+  s_m[warp][lane] = m;
+  s_s[warp][lane] = s;
+  s_z[warp][lane] = z;
+  __syncthreads();
+  if (warp == 0 && r < rows_valid) {
+    float M2 = -INFINITY, S = 0.f, Z = 0.f;
+    for (int w = 0; w < COMBINE_WARPS; ++w) {
+      const float a = s_m[w][lane], b = s_s[w][lane];
+      Z += s_z[w][lane];
+      if (a > M2) {
+        S = S * ex2(M2 - a) + b;
+        M2 = a;
+      } else if (a > -INFINITY) {
+        S += b * ex2(a - M2);
+      }
+    }
+    const float lse = (M2 + log2f(S)) * kLn2;
+    const double L = static_cast<double>(rowE[r]) - static_cast<double>(Z) +
+                     static_cast<double>(rowM[r]) * static_cast<double>(lse);
+    lse_out[r] = lse;
+    if (loss_rows_out) loss_rows_out[r] = static_cast<float>(L);
+    Lrow[r] = L;
+  }
+}
+
+// acc = (first ? 0 : acc) + sum of Lrow[0..rows) in a fixed order; on the
+// last chunk also writes the fp32 loss.
+__global__ void __launch_bounds__(1024)
+    kd_loss_reduce_kernel(const double* __restrict__ Lrow, int rows, double* acc, int first,
+                          float* loss_out) {
+  __shared__ double sm[1024];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < rows; i += 1024) s += Lrow[i];
+  sm[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 512; w > 0; w >>= 1) {
+    if (threadIdx.x < w) sm[threadIdx.x] += sm[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double tot = (first ? 0.0 : *acc) + sm[0];
+    *acc = tot;
+    if (loss_out) *loss_out = static_cast<float>(tot);
+  }
+}
+
+// dH[r, :] = scale * sum_s part[s, r, :] for the chunk's valid rows.
+__global__ void kd_dh_reduce_kernel(const float4* __restrict__ part, int S, int64_t split_stride4,
+                                    int64_t n4, float scale, float4* __restrict__ dH) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = part[i];
+    for (int s = 1; s < S; ++s) {
+      const float4 b = part[s * split_stride4 + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    a.x *= scale;
+    a.y *= scale;
+    a.z *= scale;
+    a.w *= scale;
+    dH[i] = a;
+  }
+}
+
+}  // namespace kd

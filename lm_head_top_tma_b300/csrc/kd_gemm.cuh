@@ -1,0 +1,400 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a:  D[M,N] = A[M,K] B[N,K]^T
+// with bf16 operands staged by TMA (128-byte swizzle) into a 4-deep shared-memory
+// ring and fp32 accumulators double-buffered in tensor memory (2 x 256 columns).
+//
+//   warp 0      TMA producer (one thread)
+//   warp 1      tensor-memory allocator and MMA issuer (one thread)
+//   warps 2..5  epilogue: thread i of the four warps owns accumulator row i
+//
+// Tile 128 x 256 x 64.  Operands may be K-major (the reduction index is
+// contiguous in memory) or MN-major (the row/column index is contiguous); the
+// latter lets the backward GEMMs read W, G and H in place.
+//
+// Epilogues (the loss-specific work happens on the accumulator, in registers):
+//   EPI_FWD  logits tile -> per-row online max / sum of exp over the tile's
+//            vocabulary columns, plus sum_k p_k z_k over the row's top-K ids
+//            that fall inside the tile (sorted ids, one cursor per row).  The
+//            logits never leave the SM.
+//   EPI_G    logits tile -> G = M_t exp(z - lse_t) - p at the top-K ids,
+//            rounded to bf16 and stored as the [chunk, V] operand of dH / dW.
+//   EPI_F32  fp32 store, optionally scaled and added to the destination
+//            (dW accumulation across chunks, split-K partials of dH, tests).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "kd_ptx.cuh"
+#include "kdtopk.h"
+
+namespace kd {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int GEMM_THREADS = 192;
+constexpr int SMEM_BAR_BYTES = 256;
+constexpr size_t GEMM_SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + SMEM_BAR_BYTES;
+
+enum Epi { EPI_FWD = 0, EPI_G = 1, EPI_F32 = 2 };
+
+struct GemmParams {
+  // tile grid and raster
+  int num_m, num_n, num_s;
+  int kb_total, kb_per_split;
+  int m_fast;  // 1: consecutive tile ids walk m (share a B tile), 0: walk n
+  // TMA coordinate offsets, in elements
+  int a_mn0, a_k0, b_mn0, b_k0;
+  // bounded waits / status
+  uint64_t wait_limit_ns;
+  int* status;
+  int debug_withhold_loads;
+  // EPI_FWD / EPI_G
+  int rows_valid;
+  int V, K;
+  const int32_t* sidx;  // [Cpad, K] ids ascending, padded with INT_MAX
+  const float* sp;      // [Cpad, K] probabilities in the same order
+  float* part_m;        // [num_n, ld_part] base-2 running max (z * log2 e)
+  float* part_s;        // [num_n, ld_part] sum of 2^(z log2e - max)
+  float* part_pz;       // [num_n, ld_part] sum of p z over ids in the tile
+  int ld_part;
+  const float* rowM;    // [Cpad] teacher mass per row
+  const float* lse;     // [rows_valid] lse of the chunk's rows
+  __nv_bfloat16* G;
+  int64_t ldg;
+  // EPI_F32
+  float* out;
+  int64_t ldo, split_stride;
+  int row_limit, col_limit;
+  float beta, scale;
+};
+
+__device__ __forceinline__ void decode_tile(const GemmParams& P, int tile, int& m, int& n, int& s) {
+  const int mn = P.num_m * P.num_n;
+  s = tile / mn;
+  const int r = tile - s * mn;
+  if (P.m_fast) {
+    m = r % P.num_m;
+    n = r / P.num_m;
+  } else {
+    n = r % P.num_n;
+    m = r / P.num_n;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  // barrier map: full[s], empty[s], tmem_full[2], tmem_empty[2], drain
+  const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES;
+  const uint32_t tfull0 = bar0 + 16u * STAGES, tempty0 = tfull0 + 16u;
+  const uint32_t drain_bar = tempty0 + 16u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8u * a, 1);
+      mbar_init(tempty0 + 8u * a, 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtl wc{P.wait_limit_ns, abort_flag, P.status, KD_ERR_TIMEOUT};
+  const int num_tiles = P.num_m * P.num_n * P.num_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int m, n, s;
+        decode_tile(P, tile, m, n, s);
+        const int kb0 = s * P.kb_per_split;
+        const int kb1 = min(P.kb_total, kb0 + P.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8u * stage;
+          const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_STAGE_BYTES;
+          if (!P.debug_withhold_loads) {
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            if (!A_MN) {
+              tma_load_2d(a_dst, &tmA, P.a_k0 + kb * BK, P.a_mn0 + m * BM, fb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BM / 64; ++j)
+                tma_load_2d(a_dst + j * 8192, &tmA, P.a_mn0 + m * BM + j * 64, P.a_k0 + kb * BK, fb);
+            }
+            if (!B_MN) {
+              tma_load_2d(b_dst, &tmB, P.b_k0 + kb * BK, P.b_mn0 + n * BN, fb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * 8192, &tmB, P.b_mn0 + n * BN + j * 64, P.b_k0 + kb * BK, fb);
+            }
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let copies already in flight land before the CTA exits
+        for (int s2 = 0; s2 < STAGES; ++s2)
+          if ((armed >> s2) & 1u) mbar_wait_quiet(full0 + 8u * s2, (armed_par >> s2) & 1u, P.wait_limit_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        int m, n, s;
+        decode_tile(P, tile, m, n, s);
+        const int kb0 = s * P.kb_per_split;
+        const int kb1 = min(P.kb_total, kb0 + P.kb_per_split);
+        const int acc = local & 1;
+        const uint32_t acc_par = (local >> 1) & 1;
+        if (!mbar_wait(tempty0 + 8u * acc, acc_par ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(full0 + 8u * stage, phase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_base + stage * STAGE_BYTES;
+          const uint32_t b_base = a_base + A_STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a_base + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b_base + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(b_base + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(empty0 + 8u * stage);  // frees the stage once these MMAs finish
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull0 + 8u * acc);  // accumulator ready for the epilogue
+      }
+      // every MMA issued above must be complete before tensor memory is freed
+      umma_commit(drain_bar);
+      mbar_wait_quiet(drain_bar, 0, P.wait_limit_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      int m, n, s;
+      decode_tile(P, tile, m, n, s);
+      const int acc = local & 1;
+      const uint32_t acc_par = (local >> 1) & 1;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int r = m * BM + row_in_tile;
+
+      // per-row set-up, overlapping the mainloop of this tile
+      const int32_t* ids = nullptr;
+      const float* ps = nullptr;
+      int cur = 0, cid = INT_MAX;
+      float cp = 0.f, Mr = 0.f, nl2 = 0.f;
+      bool rv = false;
+      if constexpr (EPI == EPI_FWD || EPI == EPI_G) {
+        rv = r < P.rows_valid;
+        const int n0 = n * BN;
+        ids = P.sidx + static_cast<size_t>(r) * P.K;
+        ps = P.sp + static_cast<size_t>(r) * P.K;
+        int lo = 0, hi = P.K;  // first sorted position with id >= n0
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (__ldg(ids + mid) < n0) lo = mid + 1;
+          else hi = mid;
+        }
+        cur = lo;
+        if (cur < P.K) {
+          cid = __ldg(ids + cur);
+          cp = __ldg(ps + cur);
+        }
+        if constexpr (EPI == EPI_G) {
+          if (rv) {
+            Mr = __ldg(P.rowM + r);
+            nl2 = -__ldg(P.lse + r) * kLog2e;
+          }
+        }
+      }
+
+      bool ok = mbar_wait(tfull0 + 8u * acc, acc_par, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+
+      float run_m = -INFINITY, run_s = 0.f, pz = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(taddr + c * 32, v);
+        const int col0 = n * BN + c * 32;
+        if constexpr (EPI == EPI_FWD) {
+          if (col0 < P.V) {
+            const int nv = min(32, P.V - col0);
+            float wm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nv) wm = fmaxf(wm, v[j]);
+            const float m_new = fmaxf(run_m, wm * kLog2e);
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              if (j + 0 < nv) s0 += ex2(fmaf(v[j + 0], kLog2e, -m_new));
+              if (j + 1 < nv) s1 += ex2(fmaf(v[j + 1], kLog2e, -m_new));
+              if (j + 2 < nv) s2 += ex2(fmaf(v[j + 2], kLog2e, -m_new));
+              if (j + 3 < nv) s3 += ex2(fmaf(v[j + 3], kLog2e, -m_new));
+            }
+            run_s = run_s * ex2(run_m - m_new) + ((s0 + s1) + (s2 + s3));
+            run_m = m_new;
+            while (cid < col0 + 32) {
+              const int off = cid - col0;
+              float sel = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) sel = (j == off) ? v[j] : sel;
+              pz = fmaf(cp, sel, pz);
+              ++cur;
+              cid = cur < P.K ? __ldg(ids + cur) : INT_MAX;
+              cp = cur < P.K ? __ldg(ps + cur) : 0.f;
+            }
+          }
+        } else if constexpr (EPI == EPI_G) {
+          if (col0 < P.V) {
+            float g[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) g[j] = rv ? Mr * ex2(fmaf(v[j], kLog2e, nl2)) : 0.f;
+            while (cid < col0 + 32) {
+              const int off = cid - col0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) g[j] = (j == off) ? g[j] - cp : g[j];
+              ++cur;
+              cid = cur < P.K ? __ldg(ids + cur) : INT_MAX;
+              cp = cur < P.K ? __ldg(ps + cur) : 0.f;
+            }
+            __nv_bfloat16* dst = P.G + static_cast<size_t>(r) * P.ldg + col0;
+            if (col0 + 32 <= P.V) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                d4[j] = make_uint4(pack_bf16x2(g[8 * j + 0], g[8 * j + 1]), pack_bf16x2(g[8 * j + 2], g[8 * j + 3]),
+                                   pack_bf16x2(g[8 * j + 4], g[8 * j + 5]), pack_bf16x2(g[8 * j + 6], g[8 * j + 7]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j < P.V) dst[j] = __float2bfloat16_rn(g[j]);
+            }
+          }
+        } else {  // EPI_F32
+          if (r < P.row_limit && col0 < P.col_limit) {
+            float* dst = P.out + static_cast<size_t>(s) * P.split_stride + static_cast<size_t>(r) * P.ldo + col0;
+            const bool vec = (col0 + 32 <= P.col_limit) && ((P.ldo & 3) == 0);
+            if (vec) {
+              float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float4 x = make_float4(v[4 * j] * P.scale, v[4 * j + 1] * P.scale, v[4 * j + 2] * P.scale,
+                                       v[4 * j + 3] * P.scale);
+                if (P.beta != 0.f) {
+                  const float4 o = d4[j];
+                  x.x = fmaf(P.beta, o.x, x.x);
+                  x.y = fmaf(P.beta, o.y, x.y);
+                  x.z = fmaf(P.beta, o.z, x.z);
+                  x.w = fmaf(P.beta, o.w, x.w);
+                }
+                d4[j] = x;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (col0 + j < P.col_limit) {
+                  float x = v[j] * P.scale;
+                  if (P.beta != 0.f) x = fmaf(P.beta, dst[j], x);
+                  dst[j] = x;
+                }
+              }
+            }
+          }
+        }
+      }
+      // release the accumulator buffer to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+      if constexpr (EPI == EPI_FWD) {
+        if (rv) {
+          const size_t o = static_cast<size_t>(n) * P.ld_part + r;
+          P.part_m[o] = run_m;
+          P.part_s[o] = run_s;
+          P.part_pz[o] = pz;
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace kd

@@ -1,0 +1,527 @@
+// Host side of the C ABI declared in include/kdtopk.h: argument checks,
+// workspace carving, TMA descriptor set-up and the chunk loop on the caller's
+// stream.  Method: fused, chunked top-K KL distillation loss ("Efficient
+// Knowledge Distillation for LLMs: Offline Top-K Logits and a Fused Chunked KL
+// Loss"; aimodeling.com "Second cut", thorstenmeyerai.com pipeline steps
+// "Train in chunks" / "Recompute backward").
+//
+// Per chunk of `chunk` token rows:
+//   prep      ids sorted per row, M_t, E_t, id range check
+//   forward   logits GEMM with fused online softmax partials + top-K gather
+//             (logits stay in tensor memory), combine -> lse_t, L_t, loss
+//   backward  logits GEMM again with G = M softmax - p formed in the epilogue
+//             (bf16 [chunk, V] operand), dH = G W (split-K, then a reduction),
+//             dW += G^T H (fp32 read-modify-write of the caller's dW)
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kd_aux.cuh"
+#include "kd_gemm.cuh"
+#include "kdtopk.h"
+
+namespace {
+
+using namespace kd;
+
+// ------------------------------------------------------------------ helpers
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+bool tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+// The kernels are built for sm_103a only.
+bool device_supported() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+  return major == 10 && minor == 3;
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* e = std::getenv("KD_WAIT_LIMIT_MS");
+    long ms = e ? std::atol(e) : 0;
+    if (ms <= 0) ms = 4000;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return v;
+}
+
+// ------------------------------------------------------------------ profiler
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> ev;      // pairs (start, stop)
+  std::vector<int> kind;            // per pair
+  size_t used = 0;
+  int64_t dropped = 0;
+  static constexpr size_t kPairs = 16384;
+};
+Profiler g_prof;
+
+int prof_begin(int k, cudaStream_t st) {
+  if (!g_prof.on || g_prof.used >= g_prof.kind.size()) {
+    if (g_prof.on) ++g_prof.dropped;
+    return -1;
+  }
+  const int slot = static_cast<int>(g_prof.used++);
+  g_prof.kind[slot] = k;
+  cudaEventRecord(g_prof.ev[2 * slot], st);
+  return slot;
+}
+void prof_end(int slot, cudaStream_t st) {
+  if (slot >= 0) cudaEventRecord(g_prof.ev[2 * slot + 1], st);
+}
+
+// ------------------------------------------------------------------ plan
+struct Plan {
+  int64_t T;
+  int d, V, K, C, Cpad, Kpad, nt, S, kbps_dh, nchunks;
+  int64_t ldg;
+  size_t off_status, off_sidx, off_sp, off_M, off_E, off_pm, off_ps, off_pz, off_Lrow, off_G, off_dhp, total;
+};
+
+// Split of the dH = G W reduction over V so that (row tiles x d tiles x
+// splits) fills the SMs with few partial waves.
+int choose_splits(int64_t mn_tiles, int64_t kb_total, int sms) {
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= 8; ++s) {
+    if (kb_total / s < 4) break;
+    const int64_t units = mn_tiles * s;
+    const int64_t waves = ceil_div(units, sms);
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
+    if (eff > best_eff + 0.02) {
+      best = s;
+      best_eff = eff;
+    }
+  }
+  return best;
+}
+
+kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* pl) {
+  if (T < 1 || d < 1 || V < 1 || K < 1 || chunk < 1 || (what & KD_WS_FUSED) == 0) return KD_ERR_INVALID_ARG;
+  if (K > V) return KD_ERR_INVALID_ARG;
+  if (d % 8 != 0 || K > 1024) return KD_ERR_UNSUPPORTED;
+  if (T > (int64_t(1) << 31) - 256 || static_cast<int64_t>(V) * d >= (int64_t(1) << 40)) return KD_ERR_UNSUPPORTED;
+  Plan& p = *pl;
+  p.T = T;
+  p.d = d;
+  p.V = V;
+  p.K = K;
+  p.C = static_cast<int>(std::min<int64_t>(chunk, T));
+  p.Cpad = static_cast<int>(align_up(p.C, BM));
+  p.Kpad = 32;
+  while (p.Kpad < K) p.Kpad <<= 1;
+  p.nt = static_cast<int>(ceil_div(V, BN));
+  p.ldg = static_cast<int64_t>(align_up(V, 8));
+  p.nchunks = static_cast<int>(ceil_div(T, p.C));
+  const int64_t kb_v = ceil_div(V, BK);
+  int S = choose_splits(static_cast<int64_t>(p.Cpad / BM) * ceil_div(d, BN), kb_v, current_sm_count());
+  p.kbps_dh = static_cast<int>(ceil_div(kb_v, S));
+  p.S = static_cast<int>(ceil_div(kb_v, p.kbps_dh));
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  p.off_status = take(256);  // int status + double loss accumulator
+  p.off_sidx = take(size_t(p.Cpad) * K * 4);
+  p.off_sp = take(size_t(p.Cpad) * K * 4);
+  p.off_M = take(size_t(p.Cpad) * 4);
+  p.off_E = take(size_t(p.Cpad) * 4);
+  p.off_pm = p.off_ps = p.off_pz = p.off_Lrow = 0;
+  p.off_G = p.off_dhp = 0;
+  if (what & KD_WS_FORWARD) {
+    p.off_pm = take(size_t(p.nt) * p.Cpad * 4);
+    p.off_ps = take(size_t(p.nt) * p.Cpad * 4);
+    p.off_pz = take(size_t(p.nt) * p.Cpad * 4);
+    p.off_Lrow = take(size_t(p.Cpad) * 8);
+  }
+  if (what & KD_WS_BACKWARD) {
+    p.off_G = take(size_t(p.Cpad) * p.ldg * 2);
+    p.off_dhp = take(size_t(p.S) * p.Cpad * d * 4);
+  }
+  p.total = o;
+  return KD_OK;
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+cudaError_t launch_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& P,
+                        int sms, cudaStream_t st) {
+  auto kern = kd_gemm_kernel<EPI, A_MN, B_MN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(GEMM_SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = static_cast<int64_t>(P.num_m) * P.num_n * P.num_s;
+  const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
+  const int slot = prof_begin(kind, st);
+  kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, st>>>(ta, tb, P);
+  e = cudaGetLastError();
+  prof_end(slot, st);
+  return e;
+}
+
+GemmParams base_params(int* status) {
+  GemmParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.num_s = 1;
+  P.m_fast = 1;
+  P.wait_limit_ns = wait_limit_ns();
+  P.status = status;
+  P.scale = 1.f;
+  return P;
+}
+
+enum { MODE_FWD = 1, MODE_BWD = 2 };
+
+kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const float* p, const float* lse_in,
+              int64_t T, int d, int V, int K, int chunk, float dloss, float* loss, float* lse, float* loss_rows,
+              float* dH, float* dW, int accumulate, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (!H || !W || !idx || !p || !ws) return KD_ERR_INVALID_ARG;
+  if ((mode & MODE_FWD) && (!loss || !lse)) return KD_ERR_INVALID_ARG;
+  if ((mode & MODE_BWD) && (!dH || !dW)) return KD_ERR_INVALID_ARG;
+  if (mode == MODE_BWD && !lse_in) return KD_ERR_INVALID_ARG;
+  Plan pl;
+  const int what = (mode & MODE_FWD ? KD_WS_FORWARD : 0) | (mode & MODE_BWD ? KD_WS_BACKWARD : 0);
+  kd_status rc = make_plan(T, d, V, K, chunk, what, &pl);
+  if (rc != KD_OK) return rc;
+  if (!aligned16(H) || !aligned16(W) || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+      (reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(p) & 3u) ||
+      (dH && !aligned16(dH)) || (dW && !aligned16(dW)))
+    return KD_ERR_UNSUPPORTED;
+  if (ws_bytes < pl.total) return KD_ERR_WORKSPACE;
+  if (!device_supported()) return KD_ERR_UNSUPPORTED;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  const int sms = current_sm_count();
+
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w8 + pl.off_status);
+  double* loss_acc = reinterpret_cast<double*>(w8 + pl.off_status + 8);
+  int32_t* sidx = reinterpret_cast<int32_t*>(w8 + pl.off_sidx);
+  float* sp = reinterpret_cast<float*>(w8 + pl.off_sp);
+  float* rowM = reinterpret_cast<float*>(w8 + pl.off_M);
+  float* rowE = reinterpret_cast<float*>(w8 + pl.off_E);
+  float* pm = reinterpret_cast<float*>(w8 + pl.off_pm);
+  float* ps = reinterpret_cast<float*>(w8 + pl.off_ps);
+  float* ppz = reinterpret_cast<float*>(w8 + pl.off_pz);
+  double* Lrow = reinterpret_cast<double*>(w8 + pl.off_Lrow);
+  __nv_bfloat16* G = reinterpret_cast<__nv_bfloat16*>(w8 + pl.off_G);
+  float* dhp = reinterpret_cast<float*>(w8 + pl.off_dhp);
+
+  // TMA descriptors (all bf16, 128-byte swizzle, 64-element inner boxes)
+  CUtensorMap tmH_k, tmW_k, tmG_k, tmW_mn, tmG_mn, tmH_mn;
+  const uint64_t hrow = uint64_t(d) * 2;
+  bool ok = tmap_bf16(&tmH_k, H, d, T, hrow, BK, BM) && tmap_bf16(&tmW_k, W, d, V, hrow, BK, BN);
+  if (mode & MODE_BWD) {
+    ok = ok && tmap_bf16(&tmG_k, G, V, pl.Cpad, uint64_t(pl.ldg) * 2, BK, BM) &&
+         tmap_bf16(&tmW_mn, W, d, V, hrow, 64, BK) &&
+         tmap_bf16(&tmG_mn, G, V, pl.Cpad, uint64_t(pl.ldg) * 2, 64, BK) &&
+         tmap_bf16(&tmH_mn, H, d, T, hrow, 64, BK);
+  }
+  if (!ok) return KD_ERR_CUDA;
+
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
+
+  const size_t prep_smem = size_t(PREP_WARPS) * pl.Kpad * 8;
+  if (prep_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(prep_smem)) != cudaSuccess)
+    return KD_ERR_CUDA;
+
+  for (int c = 0; c < pl.nchunks; ++c) {
+    const int64_t t0 = int64_t(c) * pl.C;
+    const int rows = static_cast<int>(std::min<int64_t>(pl.C, T - t0));
+    cudaError_t e;
+    // -------- prep
+    {
+      const int slot = prof_begin(KD_K_PREP, st);
+      kd_prep_kernel<<<static_cast<unsigned>(ceil_div(pl.Cpad, PREP_WARPS)), PREP_WARPS * 32, prep_smem, st>>>(
+          idx + t0 * K, p + t0 * K, rows, pl.Cpad, K, pl.Kpad, V, sidx, sp, rowM, rowE, status);
+      e = cudaGetLastError();
+      prof_end(slot, st);
+      if (e != cudaSuccess) return KD_ERR_CUDA;
+    }
+    GemmParams L = base_params(status);
+    L.num_m = pl.Cpad / BM;
+    L.num_n = pl.nt;
+    L.kb_total = L.kb_per_split = static_cast<int>(ceil_div(d, BK));
+    L.a_mn0 = static_cast<int>(t0);
+    L.rows_valid = rows;
+    L.V = V;
+    L.K = K;
+    L.sidx = sidx;
+    L.sp = sp;
+    // -------- forward: lse, loss
+    if (mode & MODE_FWD) {
+      GemmParams P = L;
+      P.part_m = pm;
+      P.part_s = ps;
+      P.part_pz = ppz;
+      P.ld_part = pl.Cpad;
+      if (launch_gemm<EPI_FWD, false, false>(KD_K_LOGITS_FWD, tmH_k, tmW_k, P, sms, st) != cudaSuccess)
+        return KD_ERR_CUDA;
+      const int slot = prof_begin(KD_K_COMBINE, st);
+      kd_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, 32)), COMBINE_WARPS * 32, 0, st>>>(
+          pm, ps, ppz, pl.nt, pl.Cpad, rows, rowM, rowE, lse + t0, loss_rows ? loss_rows + t0 : nullptr, Lrow);
+      kd_loss_reduce_kernel<<<1, 1024, 0, st>>>(Lrow, rows, loss_acc, c == 0 ? 1 : 0,
+                                                c == pl.nchunks - 1 ? loss : nullptr);
+      e = cudaGetLastError();
+      prof_end(slot, st);
+      if (e != cudaSuccess) return KD_ERR_CUDA;
+    }
+    // -------- backward: G, dH, dW
+    if (mode & MODE_BWD) {
+      GemmParams P = L;
+      P.rowM = rowM;
+      P.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0;
+      P.G = G;
+      P.ldg = pl.ldg;
+      if (launch_gemm<EPI_G, false, false>(KD_K_LOGITS_G, tmH_k, tmW_k, P, sms, st) != cudaSuccess)
+        return KD_ERR_CUDA;
+
+      GemmParams Q = base_params(status);  // dH partials = G W, split over V
+      Q.num_m = pl.Cpad / BM;
+      Q.num_n = static_cast<int>(ceil_div(d, BN));
+      Q.num_s = pl.S;
+      Q.kb_total = static_cast<int>(ceil_div(V, BK));
+      Q.kb_per_split = pl.kbps_dh;
+      Q.out = dhp;
+      Q.ldo = d;
+      Q.split_stride = int64_t(pl.Cpad) * d;
+      Q.row_limit = pl.Cpad;
+      Q.col_limit = d;
+      if (launch_gemm<EPI_F32, false, true>(KD_K_GEMM_DH, tmG_k, tmW_mn, Q, sms, st) != cudaSuccess)
+        return KD_ERR_CUDA;
+      {
+        const int64_t n4 = int64_t(rows) * d / 4;
+        const int slot = prof_begin(KD_K_DH_REDUCE, st);
+        kd_dh_reduce_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(n4, 256), 4L * sms)), 256, 0, st>>>(
+            reinterpret_cast<const float4*>(dhp), pl.S, Q.split_stride / 4, n4, dloss,
+            reinterpret_cast<float4*>(dH + t0 * d));
+        e = cudaGetLastError();
+        prof_end(slot, st);
+        if (e != cudaSuccess) return KD_ERR_CUDA;
+      }
+      GemmParams R = base_params(status);  // dW (+)= G^T H, fp32
+      R.num_m = static_cast<int>(ceil_div(V, BM));
+      R.num_n = static_cast<int>(ceil_div(d, BN));
+      R.m_fast = 0;
+      R.kb_total = R.kb_per_split = pl.Cpad / BK;
+      R.b_k0 = static_cast<int>(t0);
+      R.out = dW;
+      R.ldo = d;
+      R.row_limit = V;
+      R.col_limit = d;
+      R.beta = (c == 0 && !accumulate) ? 0.f : 1.f;
+      R.scale = dloss;
+      if (launch_gemm<EPI_F32, true, true>(KD_K_GEMM_DW, tmG_mn, tmH_mn, R, sms, st) != cudaSuccess)
+        return KD_ERR_CUDA;
+    }
+  }
+  return KD_OK;
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+extern "C" {
+
+size_t kd_topk_kl_workspace_size(int64_t T, int d, int V, int K, int chunk, int what) {
+  Plan pl;
+  if (make_plan(T, d, V, K, chunk, what, &pl) != KD_OK) return 0;
+  return pl.total;
+}
+
+kd_status kd_topk_kl_forward(const void* H, const void* W, const int32_t* idx, const float* p, int64_t T, int d,
+                             int V, int K, int chunk, float* loss, float* lse, float* loss_rows, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  return run(MODE_FWD, H, W, idx, p, nullptr, T, d, V, K, chunk, 1.f, loss, lse, loss_rows, nullptr, nullptr, 0,
+             workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+kd_status kd_topk_kl_backward(const void* H, const void* W, const int32_t* idx, const float* p, const float* lse,
+                              int64_t T, int d, int V, int K, int chunk, float dloss, float* dH, float* dW,
+                              int accumulate_dW, void* workspace, size_t ws_bytes, void* stream) {
+  return run(MODE_BWD, H, W, idx, p, lse, T, d, V, K, chunk, dloss, nullptr, nullptr, nullptr, dH, dW,
+             accumulate_dW, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+kd_status kd_topk_kl_fused_step(const void* H, const void* W, const int32_t* idx, const float* p, int64_t T, int d,
+                                int V, int K, int chunk, float dloss, float* loss, float* lse, float* loss_rows,
+                                float* dH, float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                                void* stream) {
+  return run(MODE_FWD | MODE_BWD, H, W, idx, p, nullptr, T, d, V, K, chunk, dloss, loss, lse, loss_rows, dH, dW,
+             accumulate_dW, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+kd_status kd_topk_kl_device_status(void* workspace, void* stream) {
+  if (!workspace) return KD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int h = 0;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return KD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KD_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
+  if (h < 0 || h > KD_ERR_CUDA) return KD_ERR_CUDA;
+  return static_cast<kd_status>(h);
+}
+
+const char* kd_status_string(kd_status s) {
+  switch (s) {
+    case KD_OK: return "ok";
+    case KD_ERR_INVALID_ARG: return "invalid argument";
+    case KD_ERR_UNSUPPORTED: return "unsupported shape, alignment or device";
+    case KD_ERR_WORKSPACE: return "workspace too small";
+    case KD_ERR_BAD_INDEX: return "teacher id outside [0, V)";
+    case KD_ERR_TIMEOUT: return "internal pipeline wait timed out";
+    case KD_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int K, int lda, int ldb, int ldd,
+                       int a_mn, int b_mn, void* workspace, size_t ws_bytes, void* stream) {
+  if (!A || !B || !D || !workspace || M < 1 || N < 1 || K < 1) return KD_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return KD_ERR_WORKSPACE;
+  if (!aligned16(A) || !aligned16(B) || (lda % 8) || (ldb % 8) || (reinterpret_cast<uintptr_t>(D) & 3u))
+    return KD_ERR_UNSUPPORTED;
+  if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldd < N) return KD_ERR_INVALID_ARG;
+  if (!device_supported()) return KD_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  CUtensorMap ta, tb;
+  bool ok = a_mn ? tmap_bf16(&ta, A, M, K, uint64_t(lda) * 2, 64, BK) : tmap_bf16(&ta, A, K, M, uint64_t(lda) * 2, BK, BM);
+  ok = ok && (b_mn ? tmap_bf16(&tb, B, N, K, uint64_t(ldb) * 2, 64, BK) : tmap_bf16(&tb, B, K, N, uint64_t(ldb) * 2, BK, BN));
+  if (!ok) return KD_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
+  GemmParams P = base_params(status);
+  P.num_m = static_cast<int>(ceil_div(M, BM));
+  P.num_n = static_cast<int>(ceil_div(N, BN));
+  P.kb_total = P.kb_per_split = static_cast<int>(ceil_div(K, BK));
+  P.out = D;
+  P.ldo = ldd;
+  P.row_limit = M;
+  P.col_limit = N;
+  const int sms = current_sm_count();
+  cudaError_t e;
+  if (!a_mn && !b_mn) e = launch_gemm<EPI_F32, false, false>(KD_K_OTHER, ta, tb, P, sms, st);
+  else if (!a_mn && b_mn) e = launch_gemm<EPI_F32, false, true>(KD_K_OTHER, ta, tb, P, sms, st);
+  else if (a_mn && !b_mn) e = launch_gemm<EPI_F32, true, false>(KD_K_OTHER, ta, tb, P, sms, st);
+  else e = launch_gemm<EPI_F32, true, true>(KD_K_OTHER, ta, tb, P, sms, st);
+  return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+kd_status kd_debug_wait_timeout(int wait_limit_ms, void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || wait_limit_ms < 1 || wait_limit_ms > 10000) return KD_ERR_INVALID_ARG;
+  if (ws_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KD_ERR_WORKSPACE;
+  if (!device_supported()) return KD_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  // The descriptors are never used to copy anything: the producer withholds every load.
+  CUtensorMap ta, tb;
+  if (!tmap_bf16(&ta, workspace, 64, 1, 128, BK, 1) || !tmap_bf16(&tb, workspace, 64, 1, 128, BK, 1))
+    return KD_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
+  GemmParams P = base_params(status);
+  P.wait_limit_ns = static_cast<uint64_t>(wait_limit_ms) * 1000000ull;
+  P.debug_withhold_loads = 1;
+  P.num_m = 1;
+  P.num_n = 1;
+  P.kb_total = P.kb_per_split = 2;
+  P.out = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 64);
+  P.ldo = 1;
+  P.row_limit = 0;  // nothing is ever written
+  P.col_limit = 0;
+  if (launch_gemm<EPI_F32, false, false>(KD_K_OTHER, ta, tb, P, 1, st) != cudaSuccess) return KD_ERR_CUDA;
+  return kd_topk_kl_device_status(workspace, stream);
+}
+
+kd_status kd_profile_enable(int on) {
+  if (on && g_prof.ev.empty()) {
+    g_prof.ev.resize(2 * Profiler::kPairs);
+    g_prof.kind.resize(Profiler::kPairs);
+    for (auto& e : g_prof.ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return KD_ERR_CUDA;
+  }
+  g_prof.on = on != 0;
+  return KD_OK;
+}
+
+int kd_profile_read(double* ms_total, int64_t* launches, int n, int reset) {
+  double ms[KD_PROF_KINDS] = {0};
+  int64_t cnt[KD_PROF_KINDS] = {0};
+  for (size_t i = 0; i < g_prof.used; ++i) {
+    float t = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) == cudaSuccess &&
+        cudaEventElapsedTime(&t, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) == cudaSuccess) {
+      ms[g_prof.kind[i]] += t;
+      cnt[g_prof.kind[i]] += 1;
+    }
+  }
+  for (int k = 0; k < n && k < KD_PROF_KINDS; ++k) {
+    if (ms_total) ms_total[k] = ms[k];
+    if (launches) launches[k] = cnt[k];
+  }
+  if (reset) {
+    g_prof.used = 0;
+    g_prof.dropped = 0;
+  }
+  return KD_PROF_KINDS;
+}
+
+const char* kd_profile_kind_name(int kind) {
+  static const char* names[KD_PROF_KINDS] = {"prep",        "logits_fwd", "combine",   "logits_g",
+                                             "gemm_dh",     "dh_reduce",  "gemm_dw",   "other"};
+  return (kind >= 0 && kind < KD_PROF_KINDS) ? names[kind] : "unknown";
+}
+
+}  // extern "C"

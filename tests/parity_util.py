@@ -1,0 +1,77 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+and compare with the fp64 oracle element by element.
+
+Tolerances.  Loss: relative error <= 1e-3; dH, dW: max-abs error <=
+2e-2 x max|ref| (the targets the method is built to).  lse and per-row loss
+are not given a target, so they get one derived from the arithmetic: every
+logit is an fp32 tensor-core sum of d bf16 products (relative error ~1e-6), the
+normaliser is an fp32 sum of V terms 2^(x) from the special-function unit
+(relative error ~2^-22 each, plus fp32 rounding over <= 256 terms per tile and
+V/256 tiles combined in fp32), so lse carries an absolute error of order 1e-5;
+1e-3 absolute leaves two orders of magnitude of margin while still catching a
+dropped tile (which moves lse by >= log(1 + 1/(V/256)) ~ 2e-3 at V = 128256),
+a missing top-K term or a wrong sign.  Per-row losses L_t = E_t - sum p z +
+M_t lse_t inherit that bound (M_t <= 1): 2e-3 absolute.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from lm_head_top_tma_b300 import api
+from oracle import kd_oracle, kd_oracle_rows
+
+LOSS_RTOL = 1e-3
+GRAD_FRAC = 2e-2
+LSE_ATOL = 1e-3
+LROW_ATOL = 2e-3
+
+
+def to_dev(idx, p, dev):
+    return (torch.as_tensor(np.ascontiguousarray(idx), dtype=torch.int32).to(dev),
+            torch.as_tensor(np.ascontiguousarray(p), dtype=torch.float32).to(dev))
+
+
+def grad_err(got: np.ndarray, ref: np.ndarray) -> float:
+    scale = float(np.abs(ref).max())
+    return float(np.abs(got - ref).max()) / max(scale, 1e-30)
+
+
+def assert_close_full(got: dict, ref: dict, what=("loss", "lse", "loss_rows", "dH", "dW")):
+    msgs = []
+    if "loss" in what:
+        rl = abs(float(got["loss"]) - ref["loss"]) / max(abs(ref["loss"]), 1e-30)
+        if not rl <= LOSS_RTOL:
+            msgs.append(f"loss rel err {rl:.3e} (gpu {float(got['loss'])!r}, ref {ref['loss']!r})")
+    if "lse" in what:
+        e = float(np.abs(got["lse"] - ref["lse"]).max())
+        if not e <= LSE_ATOL:
+            msgs.append(f"lse max abs err {e:.3e}")
+    if "loss_rows" in what and "loss_rows" in got:
+        e = float(np.abs(got["loss_rows"] - ref["loss_rows"]).max())
+        if not e <= LROW_ATOL:
+            msgs.append(f"loss_rows max abs err {e:.3e}")
+    for k in ("dH", "dW"):
+        if k in what and k in got:
+            e = grad_err(got[k], ref[k])
+            if not e <= GRAD_FRAC:
+                msgs.append(f"{k} max abs err / max|ref| = {e:.3e}")
+    assert not msgs, "; ".join(msgs)
+
+
+def fused_to_host(res: dict) -> dict:
+    torch.cuda.synchronize()
+    out = {"loss": float(res["loss"].item()), "lse": res["lse"].double().cpu().numpy(),
+           "dH": res["dH"].double().cpu().numpy(), "dW": res["dW"].double().cpu().numpy()}
+    if "loss_rows" in res:
+        out["loss_rows"] = res["loss_rows"].double().cpu().numpy()
+    return out
+
+
+def run_fused(H, W, idx_np, p_np, chunk, **kw):
+    idx, p = to_dev(idx_np, p_np, H.device)
+    return fused_to_host(api.fused_step(H, W, idx, p, chunk, loss_rows=True, **kw))
+
+
+__all__ = ["kd_oracle", "kd_oracle_rows", "to_dev", "grad_err", "assert_close_full", "fused_to_host",
+           "run_fused", "LOSS_RTOL", "GRAD_FRAC", "LSE_ATOL", "LROW_ATOL"]

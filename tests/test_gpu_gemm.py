@@ -1,0 +1,37 @@
+"""The library's tcgen05/TMA GEMM core against a plain torch reference of the
+same op (fp64 matmul of the same bf16 operands), for every operand layout the
+loss uses (K-major and MN-major A and B), with ragged M, N, K tails."""
+import math
+
+import pytest
+import torch
+
+from lm_head_top_tma_b300 import api
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(128, 256, 64), (256, 512, 128), (296, 520, 200), (384, 512, 2560), (1024, 768, 3072)]
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_matches_torch(cuda_device, a_mn, b_mn, M, N, K):
+    g = torch.Generator(device=cuda_device).manual_seed(M * 7 + N * 3 + K)
+    A = torch.randn(M, K, generator=g, device=cuda_device).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g, device=cuda_device).to(torch.bfloat16)
+    ref = (A.double() @ B.double().T).float()
+    Aop = A.t().contiguous() if a_mn else A
+    Bop = B.t().contiguous() if b_mn else B
+    D = api.gemm_bf16(Aop, Bop, M, N, K, a_mn=bool(a_mn), b_mn=bool(b_mn))
+    torch.cuda.synchronize()
+    err = (D - ref).abs().max().item()
+    assert err <= 2e-5 * math.sqrt(K) * ref.abs().max().item() + 1e-4, err
+
+
+def test_gemm_twice_same_bits(cuda_device):
+    g = torch.Generator(device=cuda_device).manual_seed(1)
+    A = torch.randn(512, 1024, generator=g, device=cuda_device).to(torch.bfloat16)
+    B = torch.randn(768, 1024, generator=g, device=cuda_device).to(torch.bfloat16)
+    d1 = api.gemm_bf16(A, B, 512, 768, 1024)
+    d2 = api.gemm_bf16(A, B, 512, 768, 1024)
+    assert torch.equal(d1, d2)
