@@ -125,6 +125,34 @@ KD_API kd_status kd_topk_kl_fused_step(const void* H, const void* W, const int32
                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * kd_topk_kl_forward for callers that cannot allocate device memory (the
+ * paper has no counterpart; this is a convenience of this library).  Same
+ * inputs, outputs and results as kd_topk_kl_forward, but the workspace is a
+ * scratch array owned by the library: KD_NOALLOC_SCRATCH_BYTES (32 MiB) of
+ * device memory that every GPU which loads the library holds until the
+ * process exits.  The call allocates nothing and calls no allocating routine.
+ *   - Sizes whose forward workspace (kd_topk_kl_workspace_size with
+ *     KD_WS_FORWARD) exceeds KD_NOALLOC_SCRATCH_BYTES are rejected with
+ *     KD_ERR_WORKSPACE before anything is launched (for example chunk 2048
+ *     fits both a 128,256- and a 201,088-word vocabulary; chunk 4096 with a
+ *     201,088-word vocabulary does not).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - Every call on a device shares the one array and finds the previous
+ *     call's contents in it; each call re-initialises what it needs.  Calls
+ *     that could overlap on the GPU (other streams, other host threads) race
+ *     on the array: order them on one stream.
+ *   - Unlike kd_topk_kl_forward it waits for `stream` before returning and
+ *     returns the device-side status (KD_OK, KD_ERR_BAD_INDEX, ...), since
+ *     the caller has no workspace to query.
+ */
+#define KD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+KD_API kd_status kd_topk_kl_forward_noalloc(const void* H, const void* W, const int32_t* idx, const float* p,
+                                            int64_t T, int d, int V, int K, int chunk,
+                                            float* loss, float* lse, float* loss_rows, void* stream);
+
+/*
  * Waits for `stream`, then returns and clears the device-side status the
  * last call on this workspace recorded (KD_OK, KD_ERR_BAD_INDEX or
  * KD_ERR_TIMEOUT), or KD_ERR_CUDA if the wait itself failed.

@@ -12,7 +12,7 @@ import torch
 
 from . import _native as N
 
-__all__ = ["workspace_size", "Workspace", "forward", "backward", "fused_step",
+__all__ = ["workspace_size", "Workspace", "forward", "forward_noalloc", "backward", "fused_step",
            "device_status", "gemm_bf16", "debug_wait_timeout", "TopKKLLoss",
            "profile_enable", "profile_read"]
 
@@ -106,6 +106,20 @@ def forward(H, W, idx, p, chunk: int, *, loss_rows: bool = False, workspace: Wor
                                      _ptr(loss), _ptr(lse), _ptr(lrows), _ptr(ws), ws.numel(), _stream(dev))
     N.check(rc, "kd_topk_kl_forward")
     _finish(ws, dev, "kd_topk_kl_forward", check)
+    return (loss, lse, lrows) if loss_rows else (loss, lse)
+
+
+def forward_noalloc(H, W, idx, p, chunk: int, *, loss_rows: bool = False):
+    """``forward`` on the library's own 32 MiB per-GPU scratch array instead of
+    a workspace, for callers that cannot allocate device memory.  Waits for
+    the stream and raises on a device-side error (bad ids)."""
+    dev, T, d, V, K = _inputs(H, W, idx, p)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    lrows = torch.empty(T, dtype=torch.float32, device=dev) if loss_rows else None
+    rc = N.load().kd_topk_kl_forward_noalloc(_ptr(H), _ptr(W), _ptr(idx), _ptr(p), T, d, V, K, int(chunk),
+                                             _ptr(loss), _ptr(lse), _ptr(lrows), _stream(dev))
+    N.check(rc, "kd_topk_kl_forward_noalloc")
     return (loss, lse, lrows) if loss_rows else (loss, lse)
 
 

@@ -525,3 +525,54 @@ const char* kd_profile_kind_name(int kind) {
 }
 
 }  // extern "C"
+
+// ==================================================================== forward without allocation
+// Some callers cannot call cudaMalloc: a plugin or custom operator that runs
+// inside another runtime's device-memory pool and is handed no allocator, a
+// process whose device-memory budget is fixed at start-up, or a loop that
+// cannot afford the device-wide synchronisation cudaMalloc / cudaFree may
+// bring.  For them the forward can run on scratch memory that the library
+// itself owns: a file-scope device array, created when the library's device
+// code is loaded on a GPU and held by every GPU that loads it until the
+// process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per GPU
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device; looked up once
+// per device (the host-side symbol is only a stand-in, never a device address).
+kd_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KD_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return KD_OK;
+}
+
+}  // namespace
+
+extern "C" kd_status kd_topk_kl_forward_noalloc(const void* H, const void* W, const int32_t* idx, const float* p,
+                                                int64_t T, int d, int V, int K, int chunk, float* loss, float* lse,
+                                                float* loss_rows, void* stream) {
+  Plan pl;
+  const kd_status rc = make_plan(T, d, V, K, chunk, KD_WS_FORWARD, &pl);
+  if (rc != KD_OK) return rc;
+  if (pl.total > kNoAllocScratchBytes) return KD_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const kd_status sc = noalloc_scratch(&scratch);
+  if (sc != KD_OK) return sc;
+  const kd_status lr = kd_topk_kl_forward(H, W, idx, p, T, d, V, K, chunk, loss, lse, loss_rows, scratch,
+                                          kNoAllocScratchBytes, stream);
+  if (lr != KD_OK) return lr;
+  return kd_topk_kl_device_status(scratch, stream);
+}
