@@ -189,6 +189,8 @@ def run_reference(args):
     from oracle import kd_oracle
 
     wl = get_workload(args.workload)
+    if args.T:
+        wl = wl.with_T(args.T)
     per_step_s = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     rows = 32
     H, W = make_hw(wl.T, wl.d, wl.V, wl.kind, wl.seed, device="cpu")
@@ -239,6 +241,8 @@ def run_kdtopk(args):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     wl = get_workload(args.workload)
+    if args.T:
+        wl = wl.with_T(args.T)
     inp = make_inputs(wl, device=dev, seed=wl.seed + rank)
     H, W = inp["H"], inp["W"]
     idx = torch.as_tensor(inp["idx"]).to(dev)
@@ -366,10 +370,11 @@ def run_kdtopk(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kdtopk", choices=["kdtopk", "reference"])
     ap.add_argument("--workload", default="longctx")
+    ap.add_argument("--T", type=int, default=None, help="override the sequence length (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
