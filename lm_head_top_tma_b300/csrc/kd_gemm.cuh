@@ -17,8 +17,11 @@
 //            logits never leave the SM.
 //   EPI_G    logits tile -> G = M_t exp(z - lse_t) - p at the top-K ids,
 //            rounded to bf16 and stored as the [chunk, V] operand of dH / dW.
-//   EPI_F32  fp32 store, optionally scaled and added to the destination
-//            (dW accumulation across chunks, split-K partials of dH, tests).
+//   EPI_F32  fp32 tile, scaled, staged through shared memory (128 x 32 slices,
+//            128-byte swizzle) and written by TMA: a plain store, or a TMA
+//            reduce-add so that L2 performs the read-modify-write of dW while
+//            the next tile's mainloop runs (dW accumulation across chunks,
+//            split-K partials of dH, tests).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -37,9 +40,18 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GEMM_THREADS = 192;
 constexpr int SMEM_BAR_BYTES = 256;
-constexpr size_t GEMM_SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + SMEM_BAR_BYTES;
+constexpr int OUT_SLICE_COLS = 32;                      // fp32 columns per TMA output slice
+constexpr int OUT_SLICE_BYTES = BM * OUT_SLICE_COLS * 4;  // 16 KB
+constexpr int OUT_STAGING_BYTES = 2 * OUT_SLICE_BYTES;
+constexpr int EPI_WARPS = 4;
+constexpr uint32_t EPI_BAR_ID = 1;  // named barrier of the epilogue warps
 
 enum Epi { EPI_FWD = 0, EPI_G = 1, EPI_F32 = 2 };
+
+__host__ __device__ constexpr int staging_bytes(int epi) { return epi == EPI_F32 ? OUT_STAGING_BYTES : 0; }
+__host__ __device__ constexpr size_t gemm_smem_bytes(int epi) {
+  return 1024 + size_t(STAGES) * STAGE_BYTES + staging_bytes(epi) + SMEM_BAR_BYTES;
+}
 
 struct GemmParams {
   // tile grid and raster
@@ -65,11 +77,11 @@ struct GemmParams {
   const float* lse;     // [rows_valid] lse of the chunk's rows
   __nv_bfloat16* G;
   int64_t ldg;
-  // EPI_F32
-  float* out;
-  int64_t ldo, split_stride;
-  int row_limit, col_limit;
-  float beta, scale;
+  // EPI_F32: output tile (m, n, s) goes to rows out_row0 + s * split_rows + m * BM,
+  // columns n * BN of the fp32 tensor map; reduce_add adds instead of storing
+  int out_row0, split_rows;
+  int reduce_add;
+  float scale;
 };
 
 __device__ __forceinline__ void decode_tile(const GemmParams& P, int tile, int& m, int& n, int& s) {
@@ -93,11 +105,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams P) {
+                   const __grid_constant__ CUtensorMap tmD, const GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + staging_bytes(EPI));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -125,6 +138,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if constexpr (EPI == EPI_F32) prefetch_tmap(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -237,6 +251,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_in_tile = q * 32 + lane;
+    const bool out_leader = threadIdx.x == 2 * 32;  // issues the epilogue's TMA stores
+    const uint32_t staging_base = smem_u32(staging);
+    uint32_t slice = 0;  // running count of output slices (alternates staging buffers)
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       int m, n, s;
@@ -277,7 +294,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
 
       bool ok = mbar_wait(tfull0 + 8u * acc, acc_par, wc);
-      ok = __all_sync(0xffffffffu, ok);
+      // all four epilogue warps must take the same decision: the fp32 path
+      // synchronises them on a named barrier below
+      if constexpr (EPI == EPI_F32) ok = named_bar_and(EPI_BAR_ID, EPI_WARPS * 32, ok);
+      else ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
 
@@ -343,35 +363,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           }
         } else {  // EPI_F32
-          if (r < P.row_limit && col0 < P.col_limit) {
-            float* dst = P.out + static_cast<size_t>(s) * P.split_stride + static_cast<size_t>(r) * P.ldo + col0;
-            const bool vec = (col0 + 32 <= P.col_limit) && ((P.ldo & 3) == 0);
-            if (vec) {
-              float4* d4 = reinterpret_cast<float4*>(dst);
+          const uint32_t buf = staging_base + (slice & 1u) * OUT_SLICE_BYTES;
+          if (out_leader) bulk_wait_read1();  // the store that last read `buf` is done with it
+          named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
+          const uint32_t row_addr = buf + row_in_tile * 128;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                float4 x = make_float4(v[4 * j] * P.scale, v[4 * j + 1] * P.scale, v[4 * j + 2] * P.scale,
-                                       v[4 * j + 3] * P.scale);
-                if (P.beta != 0.f) {
-                  const float4 o = d4[j];
-                  x.x = fmaf(P.beta, o.x, x.x);
-                  x.y = fmaf(P.beta, o.y, x.y);
-                  x.z = fmaf(P.beta, o.z, x.z);
-                  x.w = fmaf(P.beta, o.w, x.w);
-                }
-                d4[j] = x;
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                if (col0 + j < P.col_limit) {
-                  float x = v[j] * P.scale;
-                  if (P.beta != 0.f) x = fmaf(P.beta, dst[j], x);
-                  dst[j] = x;
-                }
-              }
-            }
+          for (int j = 0; j < 8; ++j)  // 16-byte chunk j of the row goes to chunk j ^ (row % 8)
+            st_shared_v4(row_addr + ((j ^ (row_in_tile & 7)) << 4), v[4 * j] * P.scale,
+                         v[4 * j + 1] * P.scale, v[4 * j + 2] * P.scale, v[4 * j + 3] * P.scale);
+          fence_proxy_async_smem();
+          named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
+          if (out_leader) {
+            const int y = P.out_row0 + s * P.split_rows + m * BM;
+            if (P.reduce_add) tma_reduce_add_2d(&tmD, col0, y, buf);
+            else tma_store_2d(&tmD, col0, y, buf);
+            bulk_commit();
           }
+          ++slice;
         }
       }
       // release the accumulator buffer to the MMA warp
@@ -389,6 +397,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
 
+  if constexpr (EPI == EPI_F32) {
+    if (threadIdx.x == 2 * 32) bulk_wait0();  // output stores complete before the CTA exits
+  }
   __syncthreads();
   if (warp == 1) {
     __syncwarp();

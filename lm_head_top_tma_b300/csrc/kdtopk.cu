@@ -64,6 +64,19 @@ bool tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 tensor map for the GEMM outputs: 32-column x 128-row boxes, 128-byte swizzle.
+bool tmap_f32_out(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(OUT_SLICE_COLS), static_cast<cuuint32_t>(BM)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int current_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -196,16 +209,16 @@ kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* p
 }
 
 template <int EPI, bool A_MN, bool B_MN>
-cudaError_t launch_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& P,
-                        int sms, cudaStream_t st) {
+cudaError_t launch_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                        const GemmParams& P, int sms, cudaStream_t st) {
   auto kern = kd_gemm_kernel<EPI, A_MN, B_MN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(GEMM_SMEM_BYTES));
+  constexpr size_t smem = gemm_smem_bytes(EPI);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int64_t tiles = static_cast<int64_t>(P.num_m) * P.num_n * P.num_s;
   const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
   const int slot = prof_begin(kind, st);
-  kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, st>>>(ta, tb, P);
+  kern<<<grid, GEMM_THREADS, smem, st>>>(ta, tb, td, P);
   e = cudaGetLastError();
   prof_end(slot, st);
   return e;
@@ -259,14 +272,16 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   float* dhp = reinterpret_cast<float*>(w8 + pl.off_dhp);
 
   // TMA descriptors (all bf16, 128-byte swizzle, 64-element inner boxes)
-  CUtensorMap tmH_k, tmW_k, tmG_k, tmW_mn, tmG_mn, tmH_mn;
+  CUtensorMap tmH_k, tmW_k, tmG_k, tmW_mn, tmG_mn, tmH_mn, tmDhp, tmDW;
   const uint64_t hrow = uint64_t(d) * 2;
   bool ok = tmap_bf16(&tmH_k, H, d, T, hrow, BK, BM) && tmap_bf16(&tmW_k, W, d, V, hrow, BK, BN);
   if (mode & MODE_BWD) {
     ok = ok && tmap_bf16(&tmG_k, G, V, pl.Cpad, uint64_t(pl.ldg) * 2, BK, BM) &&
          tmap_bf16(&tmW_mn, W, d, V, hrow, 64, BK) &&
          tmap_bf16(&tmG_mn, G, V, pl.Cpad, uint64_t(pl.ldg) * 2, 64, BK) &&
-         tmap_bf16(&tmH_mn, H, d, T, hrow, 64, BK);
+         tmap_bf16(&tmH_mn, H, d, T, hrow, 64, BK) &&
+         tmap_f32_out(&tmDhp, dhp, d, uint64_t(pl.S) * pl.Cpad, uint64_t(d) * 4) &&
+         tmap_f32_out(&tmDW, dW, d, V, uint64_t(d) * 4);
   }
   if (!ok) return KD_ERR_CUDA;
 
@@ -308,7 +323,7 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       P.part_s = ps;
       P.part_pz = ppz;
       P.ld_part = pl.Cpad;
-      if (launch_gemm<EPI_FWD, false, false>(KD_K_LOGITS_FWD, tmH_k, tmW_k, P, sms, st) != cudaSuccess)
+      if (launch_gemm<EPI_FWD, false, false>(KD_K_LOGITS_FWD, tmH_k, tmW_k, tmH_k, P, sms, st) != cudaSuccess)
         return KD_ERR_CUDA;
       const int slot = prof_begin(KD_K_COMBINE, st);
       kd_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, 32)), COMBINE_WARPS * 32, 0, st>>>(
@@ -326,7 +341,7 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       P.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0;
       P.G = G;
       P.ldg = pl.ldg;
-      if (launch_gemm<EPI_G, false, false>(KD_K_LOGITS_G, tmH_k, tmW_k, P, sms, st) != cudaSuccess)
+      if (launch_gemm<EPI_G, false, false>(KD_K_LOGITS_G, tmH_k, tmW_k, tmH_k, P, sms, st) != cudaSuccess)
         return KD_ERR_CUDA;
 
       GemmParams Q = base_params(status);  // dH partials = G W, split over V
@@ -335,18 +350,14 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       Q.num_s = pl.S;
       Q.kb_total = static_cast<int>(ceil_div(V, BK));
       Q.kb_per_split = pl.kbps_dh;
-      Q.out = dhp;
-      Q.ldo = d;
-      Q.split_stride = int64_t(pl.Cpad) * d;
-      Q.row_limit = pl.Cpad;
-      Q.col_limit = d;
-      if (launch_gemm<EPI_F32, false, true>(KD_K_GEMM_DH, tmG_k, tmW_mn, Q, sms, st) != cudaSuccess)
+      Q.split_rows = pl.Cpad;
+      if (launch_gemm<EPI_F32, false, true>(KD_K_GEMM_DH, tmG_k, tmW_mn, tmDhp, Q, sms, st) != cudaSuccess)
         return KD_ERR_CUDA;
       {
         const int64_t n4 = int64_t(rows) * d / 4;
         const int slot = prof_begin(KD_K_DH_REDUCE, st);
         kd_dh_reduce_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(n4, 256), 4L * sms)), 256, 0, st>>>(
-            reinterpret_cast<const float4*>(dhp), pl.S, Q.split_stride / 4, n4, dloss,
+            reinterpret_cast<const float4*>(dhp), pl.S, int64_t(pl.Cpad) * d / 4, n4, dloss,
             reinterpret_cast<float4*>(dH + t0 * d));
         e = cudaGetLastError();
         prof_end(slot, st);
@@ -358,13 +369,9 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       R.m_fast = 0;
       R.kb_total = R.kb_per_split = pl.Cpad / BK;
       R.b_k0 = static_cast<int>(t0);
-      R.out = dW;
-      R.ldo = d;
-      R.row_limit = V;
-      R.col_limit = d;
-      R.beta = (c == 0 && !accumulate) ? 0.f : 1.f;
+      R.reduce_add = (c == 0 && !accumulate) ? 0 : 1;  // first chunk stores, the rest add in L2
       R.scale = dloss;
-      if (launch_gemm<EPI_F32, true, true>(KD_K_GEMM_DW, tmG_mn, tmH_mn, R, sms, st) != cudaSuccess)
+      if (launch_gemm<EPI_F32, true, true>(KD_K_GEMM_DW, tmG_mn, tmH_mn, tmDW, R, sms, st) != cudaSuccess)
         return KD_ERR_CUDA;
     }
   }
@@ -432,7 +439,7 @@ kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int
                        int a_mn, int b_mn, void* workspace, size_t ws_bytes, void* stream) {
   if (!A || !B || !D || !workspace || M < 1 || N < 1 || K < 1) return KD_ERR_INVALID_ARG;
   if (ws_bytes < 256) return KD_ERR_WORKSPACE;
-  if (!aligned16(A) || !aligned16(B) || (lda % 8) || (ldb % 8) || (reinterpret_cast<uintptr_t>(D) & 3u))
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (lda % 8) || (ldb % 8) || (ldd % 4))
     return KD_ERR_UNSUPPORTED;
   if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldd < N) return KD_ERR_INVALID_ARG;
   if (!device_supported()) return KD_ERR_UNSUPPORTED;
@@ -441,22 +448,20 @@ kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int
   CUtensorMap ta, tb;
   bool ok = a_mn ? tmap_bf16(&ta, A, M, K, uint64_t(lda) * 2, 64, BK) : tmap_bf16(&ta, A, K, M, uint64_t(lda) * 2, BK, BM);
   ok = ok && (b_mn ? tmap_bf16(&tb, B, N, K, uint64_t(ldb) * 2, 64, BK) : tmap_bf16(&tb, B, K, N, uint64_t(ldb) * 2, BK, BN));
+  CUtensorMap td;
+  ok = ok && tmap_f32_out(&td, D, N, M, uint64_t(ldd) * 4);
   if (!ok) return KD_ERR_CUDA;
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
   GemmParams P = base_params(status);
   P.num_m = static_cast<int>(ceil_div(M, BM));
   P.num_n = static_cast<int>(ceil_div(N, BN));
   P.kb_total = P.kb_per_split = static_cast<int>(ceil_div(K, BK));
-  P.out = D;
-  P.ldo = ldd;
-  P.row_limit = M;
-  P.col_limit = N;
   const int sms = current_sm_count();
   cudaError_t e;
-  if (!a_mn && !b_mn) e = launch_gemm<EPI_F32, false, false>(KD_K_OTHER, ta, tb, P, sms, st);
-  else if (!a_mn && b_mn) e = launch_gemm<EPI_F32, false, true>(KD_K_OTHER, ta, tb, P, sms, st);
-  else if (a_mn && !b_mn) e = launch_gemm<EPI_F32, true, false>(KD_K_OTHER, ta, tb, P, sms, st);
-  else e = launch_gemm<EPI_F32, true, true>(KD_K_OTHER, ta, tb, P, sms, st);
+  if (!a_mn && !b_mn) e = launch_gemm<EPI_F32, false, false>(KD_K_OTHER, ta, tb, td, P, sms, st);
+  else if (!a_mn && b_mn) e = launch_gemm<EPI_F32, false, true>(KD_K_OTHER, ta, tb, td, P, sms, st);
+  else if (a_mn && !b_mn) e = launch_gemm<EPI_F32, true, false>(KD_K_OTHER, ta, tb, td, P, sms, st);
+  else e = launch_gemm<EPI_F32, true, true>(KD_K_OTHER, ta, tb, td, P, sms, st);
   return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
@@ -467,8 +472,9 @@ kd_status kd_debug_wait_timeout(int wait_limit_ms, void* workspace, size_t ws_by
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = static_cast<int*>(workspace);
   // The descriptors are never used to copy anything: the producer withholds every load.
-  CUtensorMap ta, tb;
-  if (!tmap_bf16(&ta, workspace, 64, 1, 128, BK, 1) || !tmap_bf16(&tb, workspace, 64, 1, 128, BK, 1))
+  CUtensorMap ta, tb, td;
+  if (!tmap_bf16(&ta, workspace, 64, 1, 128, BK, 1) || !tmap_bf16(&tb, workspace, 64, 1, 128, BK, 1) ||
+      !tmap_f32_out(&td, workspace, 32, 1, 128))
     return KD_ERR_CUDA;
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
   GemmParams P = base_params(status);
@@ -477,11 +483,7 @@ kd_status kd_debug_wait_timeout(int wait_limit_ms, void* workspace, size_t ws_by
   P.num_m = 1;
   P.num_n = 1;
   P.kb_total = P.kb_per_split = 2;
-  P.out = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 64);
-  P.ldo = 1;
-  P.row_limit = 0;  // nothing is ever written
-  P.col_limit = 0;
-  if (launch_gemm<EPI_F32, false, false>(KD_K_OTHER, ta, tb, P, 1, st) != cudaSuccess) return KD_ERR_CUDA;
+  if (launch_gemm<EPI_F32, false, false>(KD_K_OTHER, ta, tb, td, P, 1, st) != cudaSuccess) return KD_ERR_CUDA;
   return kd_topk_kl_device_status(workspace, stream);
 }
 
