@@ -38,7 +38,11 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 
 # DRAM traffic of the dominant kernel from an ncu capture (see profiles/);
 # reported only while the kernel sources still hash to what was captured.
-TRAFFIC = {"kernel": None, "bytes_per_launch": None, "src_sha": None}
+# dW GEMM, one 2048-row chunk of the long-context head: the first chunk stores dW
+# (2.060 GB), every later chunk reduce-adds into it (3.631 GB); bench lines
+# weight the two by the launch mix (profiles/gemm_traffic_longctx_chunk2048.md).
+TRAFFIC = {"kernel": "gemm_dw", "workload": "longctx", "store_bytes": 538509824 + 1521478912,
+           "accumulate_bytes": 2115711744 + 1515372288, "src_sha": "36c65d452f0810f7"}
 KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300/csrc/kd_ptx.cuh",
                   "lm_head_top_tma_b300/csrc/kdtopk.cu"]
 
@@ -325,8 +329,10 @@ def run_kdtopk(args):
     dom_ms, dom_n = prof[dom]
     per_launch_flops = 2.0 * min(C, T) * V * d if dom in gemm_kinds else None
     achieved = per_launch_flops / (dom_ms / dom_n / 1e3) / 1e12 if per_launch_flops and dom_n else None
-    traffic = TRAFFIC["bytes_per_launch"] if (TRAFFIC["kernel"] == dom and
-                                              TRAFFIC["src_sha"] == kernel_src_sha()) else None
+    traffic = None
+    if (TRAFFIC["kernel"] == dom and TRAFFIC["workload"] == wl.name and C == get_workload(wl.name).chunk
+            and TRAFFIC["src_sha"] == kernel_src_sha()):
+        traffic = (TRAFFIC["store_bytes"] + (nchunks - 1) * TRAFFIC["accumulate_bytes"]) / nchunks
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sustained"],
                 "unit": "TFLOP/s", "frac": (achieved / peaks["bf16_sustained"]) if achieved else None,
                 "traffic": traffic, "peak_kind": f"bf16 sustained ({peaks['source']})",
@@ -367,6 +373,54 @@ def run_kdtopk(args):
     return 0
 
 
+def run_sweep(args):
+    """Output-head-only scaling sweep (d 4096, V 128256, K 100, chunk 4096, T 4K..256K):
+    one JSON line per T with tokens/s, TFLOP/s, library workspace and device peak bytes."""
+    import torch
+
+    from lm_head_top_tma_b300 import _native as N
+    from lm_head_top_tma_b300 import api
+    from lm_head_top_tma_b300.inputs import SWEEP_T, make_inputs, sweep_workload
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    for T in SWEEP_T:
+        wl = sweep_workload(T)
+        inp = make_inputs(wl, device=dev)
+        H, W = inp["H"], inp["W"]
+        idx = torch.as_tensor(inp["idx"]).to(dev)
+        p = torch.as_tensor(inp["p"]).to(dev)
+        del inp
+        torch.cuda.synchronize(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        work = api.Workspace(dev)
+        out = {"loss": torch.empty(1, device=dev), "lse": torch.empty(T, device=dev),
+               "dH": torch.empty(T, wl.d, device=dev), "dW": torch.empty(wl.V, wl.d, device=dev)}
+        for _ in range(max(1, args.warmup)):
+            api.fused_step(H, W, idx, p, wl.chunk, workspace=work, out=out, check=False)
+        N.check(api.device_status(work.buf, dev), "sweep warm-up")
+        steps = max(1, min(args.steps, 5))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(steps):
+            api.fused_step(H, W, idx, p, wl.chunk, workspace=work, out=out, check=False)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        peak = torch.cuda.max_memory_allocated(dev)
+        print(json.dumps({
+            "sweep": wl.name, "T": T, "d": wl.d, "V": wl.V, "K": wl.K, "chunk": wl.chunk,
+            "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3),
+            "tflops_8TVd": 8.0 * T * wl.V * wl.d / (ms / 1e3) / 1e12,
+            "workspace_bytes": work.nbytes, "peak_bytes": peak, "inputs_bytes": base,
+            "peak_GiB": peak / 2**30}), flush=True)
+        del H, W, idx, p, out, work
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -377,7 +431,10 @@ def main():
     ap.add_argument("--T", type=int, default=None, help="override the sequence length (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="output-head-only T sweep, one line per T")
     args = ap.parse_args()
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_kdtopk(args)

@@ -16,7 +16,9 @@
 //            that fall inside the tile (sorted ids, one cursor per row).  The
 //            logits never leave the SM.
 //   EPI_G    logits tile -> G = M_t exp(z - lse_t) - p at the top-K ids,
-//            rounded to bf16 and stored as the [chunk, V] operand of dH / dW.
+//            rounded to bf16, staged as 128 x 64 swizzled slices and written
+//            by TMA as the [chunk, V] operand of dH / dW (TMA clips the
+//            vocabulary tail).
 //   EPI_F32  fp32 tile, scaled, staged through shared memory (128 x 32 slices,
 //            128-byte swizzle) and written by TMA: a plain store, or a TMA
 //            reduce-add so that L2 performs the read-modify-write of dW while
@@ -40,15 +42,16 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GEMM_THREADS = 192;
 constexpr int SMEM_BAR_BYTES = 256;
-constexpr int OUT_SLICE_COLS = 32;                      // fp32 columns per TMA output slice
-constexpr int OUT_SLICE_BYTES = BM * OUT_SLICE_COLS * 4;  // 16 KB
+constexpr int OUT_SLICE_COLS = 32;                        // fp32 columns per TMA output slice
+constexpr int OUT_SLICE_BYTES = BM * 128;                 // 16 KB: 128 rows x 128 bytes
+constexpr int G_SLICE_COLS = 64;                          // bf16 columns per TMA output slice
 constexpr int OUT_STAGING_BYTES = 2 * OUT_SLICE_BYTES;
 constexpr int EPI_WARPS = 4;
 constexpr uint32_t EPI_BAR_ID = 1;  // named barrier of the epilogue warps
 
 enum Epi { EPI_FWD = 0, EPI_G = 1, EPI_F32 = 2 };
 
-__host__ __device__ constexpr int staging_bytes(int epi) { return epi == EPI_F32 ? OUT_STAGING_BYTES : 0; }
+__host__ __device__ constexpr int staging_bytes(int epi) { return epi == EPI_FWD ? 0 : OUT_STAGING_BYTES; }
 __host__ __device__ constexpr size_t gemm_smem_bytes(int epi) {
   return 1024 + size_t(STAGES) * STAGE_BYTES + staging_bytes(epi) + SMEM_BAR_BYTES;
 }
@@ -75,8 +78,6 @@ struct GemmParams {
   int ld_part;
   const float* rowM;    // [Cpad] teacher mass per row
   const float* lse;     // [rows_valid] lse of the chunk's rows
-  __nv_bfloat16* G;
-  int64_t ldg;
   // EPI_F32: output tile (m, n, s) goes to rows out_row0 + s * split_rows + m * BM,
   // columns n * BN of the fp32 tensor map; reduce_add adds instead of storing
   int out_row0, split_rows;
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if constexpr (EPI == EPI_F32) prefetch_tmap(&tmD);
+    if constexpr (EPI != EPI_FWD) prefetch_tmap(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -294,9 +295,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
 
       bool ok = mbar_wait(tfull0 + 8u * acc, acc_par, wc);
-      // all four epilogue warps must take the same decision: the fp32 path
-      // synchronises them on a named barrier below
-      if constexpr (EPI == EPI_F32) ok = named_bar_and(EPI_BAR_ID, EPI_WARPS * 32, ok);
+      // all four epilogue warps must take the same decision: the TMA-store
+      // paths synchronise them on a named barrier below
+      if constexpr (EPI != EPI_FWD) ok = named_bar_and(EPI_BAR_ID, EPI_WARPS * 32, ok);
       else ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -337,30 +338,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           }
         } else if constexpr (EPI == EPI_G) {
-          if (col0 < P.V) {
-            float g[32];
+          // two 32-column windows fill one 128 x 64 bf16 slice of the staging buffer
+          const uint32_t buf = staging_base + (slice & 1u) * OUT_SLICE_BYTES;
+          if ((c & 1) == 0) {
+            if (out_leader) bulk_wait_read1();  // the store that last read `buf` is done with it
+            named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
+          }
+          float g[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) g[j] = rv ? Mr * ex2(fmaf(v[j], kLog2e, nl2)) : 0.f;
-            while (cid < col0 + 32) {
-              const int off = cid - col0;
+          for (int j = 0; j < 32; ++j) g[j] = rv ? Mr * ex2(fmaf(v[j], kLog2e, nl2)) : 0.f;
+          while (cid < col0 + 32) {
+            const int off = cid - col0;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) g[j] = (j == off) ? g[j] - cp : g[j];
-              ++cur;
-              cid = cur < P.K ? __ldg(ids + cur) : INT_MAX;
-              cp = cur < P.K ? __ldg(ps + cur) : 0.f;
+            for (int j = 0; j < 32; ++j) g[j] = (j == off) ? g[j] - cp : g[j];
+            ++cur;
+            cid = cur < P.K ? __ldg(ids + cur) : INT_MAX;
+            cp = cur < P.K ? __ldg(ps + cur) : 0.f;
+          }
+          const uint32_t row_addr = buf + row_in_tile * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // 16-byte chunk (c & 1) * 4 + j of the row, swizzled
+            const uint32_t chunk = static_cast<uint32_t>(((c & 1) << 2) + j) ^ static_cast<uint32_t>(row_in_tile & 7);
+            st_shared_v4_b32(row_addr + (chunk << 4), pack_bf16x2(g[8 * j + 0], g[8 * j + 1]),
+                             pack_bf16x2(g[8 * j + 2], g[8 * j + 3]), pack_bf16x2(g[8 * j + 4], g[8 * j + 5]),
+                             pack_bf16x2(g[8 * j + 6], g[8 * j + 7]));
+          }
+          if (c & 1) {
+            fence_proxy_async_smem();
+            named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
+            if (out_leader) {
+              tma_store_2d(&tmD, n * BN + (c >> 1) * G_SLICE_COLS, m * BM, buf);
+              bulk_commit();
             }
-            __nv_bfloat16* dst = P.G + static_cast<size_t>(r) * P.ldg + col0;
-            if (col0 + 32 <= P.V) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                d4[j] = make_uint4(pack_bf16x2(g[8 * j + 0], g[8 * j + 1]), pack_bf16x2(g[8 * j + 2], g[8 * j + 3]),
-                                   pack_bf16x2(g[8 * j + 4], g[8 * j + 5]), pack_bf16x2(g[8 * j + 6], g[8 * j + 7]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col0 + j < P.V) dst[j] = __float2bfloat16_rn(g[j]);
-            }
+            ++slice;
           }
         } else {  // EPI_F32
           const uint32_t buf = staging_base + (slice & 1u) * OUT_SLICE_BYTES;
@@ -397,7 +407,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
 
-  if constexpr (EPI == EPI_F32) {
+  if constexpr (EPI != EPI_FWD) {
     if (threadIdx.x == 2 * 32) bulk_wait0();  // output stores complete before the CTA exits
   }
   __syncthreads();

@@ -339,9 +339,7 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       GemmParams P = L;
       P.rowM = rowM;
       P.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0;
-      P.G = G;
-      P.ldg = pl.ldg;
-      if (launch_gemm<EPI_G, false, false>(KD_K_LOGITS_G, tmH_k, tmW_k, tmH_k, P, sms, st) != cudaSuccess)
+      if (launch_gemm<EPI_G, false, false>(KD_K_LOGITS_G, tmH_k, tmW_k, tmG_k, P, sms, st) != cudaSuccess)
         return KD_ERR_CUDA;
 
       GemmParams Q = base_params(status);  // dH partials = G W, split over V
