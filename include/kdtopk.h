@@ -85,6 +85,10 @@ typedef enum kd_status {
  * gradient operand and [chunk, V/256] softmax partials) is reused chunk after
  * chunk, so memory grows linearly in T only through the caller's own inputs
  * and outputs.  Returns 0 for invalid sizes.
+ * When chunk is a multiple of 128 the backward keeps G for a group of
+ * consecutive chunks (up to 4096 rows, at most 4 chunks; environment variable
+ * KD_DW_GROUP_ROWS, read once per process, changes the row target, 0 turns it
+ * off) and runs one dW GEMM per group; the workspace size includes it.
  */
 KD_API size_t kd_topk_kl_workspace_size(int64_t T, int d, int V, int K, int chunk, int what);
 

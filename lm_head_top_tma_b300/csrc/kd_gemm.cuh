@@ -79,7 +79,8 @@ struct GemmParams {
   const float* rowM;    // [Cpad] teacher mass per row
   const float* lse;     // [rows_valid] lse of the chunk's rows
   // EPI_F32: output tile (m, n, s) goes to rows out_row0 + s * split_rows + m * BM,
-  // columns n * BN of the fp32 tensor map; reduce_add adds instead of storing
+  // columns n * BN of the fp32 tensor map; reduce_add adds instead of storing.
+  // EPI_G: tile rows go to out_row0 + m * BM of the G tensor map.
   int out_row0, split_rows;
   int reduce_add;
   float scale;
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             fence_proxy_async_smem();
             named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
             if (out_leader) {
-              tma_store_2d(&tmD, n * BN + (c >> 1) * G_SLICE_COLS, m * BM, buf);
+              tma_store_2d(&tmD, n * BN + (c >> 1) * G_SLICE_COLS, P.out_row0 + m * BM, buf);
               bulk_commit();
             }
             ++slice;

@@ -99,6 +99,21 @@ bool device_supported() {
   return major == 10 && minor == 3;
 }
 
+// Rows of G that one dW = G^T H launch reduces over.  A dW tile's mainloop is
+// only K = chunk rows long while its epilogue read-modify-writes a 128 x 256
+// fp32 tile of dW, so for short chunks the epilogue cannot hide behind the
+// tensor cores; grouping consecutive chunks (G kept for the whole group)
+// lengthens K and divides dW's HBM traffic per chunk.  KD_DW_GROUP_ROWS
+// overrides the default 4096 rows (at most 4 chunks; 0 or fewer rows than two
+// chunks: no grouping).
+int dw_group_rows() {
+  static int v = [] {
+    const char* e = std::getenv("KD_DW_GROUP_ROWS");
+    return e ? std::atoi(e) : 4096;
+  }();
+  return v;
+}
+
 uint64_t wait_limit_ns() {
   static uint64_t v = [] {
     const char* e = std::getenv("KD_WAIT_LIMIT_MS");
@@ -138,6 +153,7 @@ void prof_end(int slot, cudaStream_t st) {
 struct Plan {
   int64_t T;
   int d, V, K, C, Cpad, Kpad, nt, S, kbps_dh, nchunks;
+  int dw_group;  // chunks whose G rows one dW GEMM consumes (K = dw_group * C)
   int64_t ldg;
   size_t off_status, off_sidx, off_sp, off_M, off_E, off_pm, off_ps, off_pz, off_Lrow, off_G, off_dhp, total;
 };
@@ -177,6 +193,9 @@ kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* p
   p.nt = static_cast<int>(ceil_div(V, BN));
   p.ldg = static_cast<int64_t>(align_up(V, 8));
   p.nchunks = static_cast<int>(ceil_div(T, p.C));
+  // grouping needs the chunks' G rows to line up with H rows: chunk == Cpad
+  p.dw_group = (p.C == p.Cpad) ? std::min(4, std::max(1, dw_group_rows() / p.C)) : 1;
+  p.dw_group = std::min(p.dw_group, p.nchunks);
   const int64_t kb_v = ceil_div(V, BK);
   int S = choose_splits(static_cast<int64_t>(p.Cpad / BM) * ceil_div(d, BN), kb_v, current_sm_count());
   p.kbps_dh = static_cast<int>(ceil_div(kb_v, S));
@@ -201,7 +220,7 @@ kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* p
     p.off_Lrow = take(size_t(p.Cpad) * 8);
   }
   if (what & KD_WS_BACKWARD) {
-    p.off_G = take(size_t(p.Cpad) * p.ldg * 2);
+    p.off_G = take(size_t(p.dw_group) * p.Cpad * p.ldg * 2);
     p.off_dhp = take(size_t(p.S) * p.Cpad * d * 4);
   }
   p.total = o;
@@ -276,9 +295,10 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   const uint64_t hrow = uint64_t(d) * 2;
   bool ok = tmap_bf16(&tmH_k, H, d, T, hrow, BK, BM) && tmap_bf16(&tmW_k, W, d, V, hrow, BK, BN);
   if (mode & MODE_BWD) {
-    ok = ok && tmap_bf16(&tmG_k, G, V, pl.Cpad, uint64_t(pl.ldg) * 2, BK, BM) &&
+    const uint64_t grows = uint64_t(pl.dw_group) * pl.Cpad;  // G rows held in the workspace
+    ok = ok && tmap_bf16(&tmG_k, G, V, grows, uint64_t(pl.ldg) * 2, BK, BM) &&
          tmap_bf16(&tmW_mn, W, d, V, hrow, 64, BK) &&
-         tmap_bf16(&tmG_mn, G, V, pl.Cpad, uint64_t(pl.ldg) * 2, 64, BK) &&
+         tmap_bf16(&tmG_mn, G, V, grows, uint64_t(pl.ldg) * 2, 64, BK) &&
          tmap_bf16(&tmH_mn, H, d, T, hrow, 64, BK) &&
          tmap_f32_out(&tmDhp, dhp, d, uint64_t(pl.S) * pl.Cpad, uint64_t(d) * 4) &&
          tmap_f32_out(&tmDW, dW, d, V, uint64_t(d) * 4);
@@ -336,7 +356,9 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
     }
     // -------- backward: G, dH, dW
     if (mode & MODE_BWD) {
+      const int gslot = c % pl.dw_group;  // this chunk's G rows: [gslot * Cpad, +Cpad)
       GemmParams P = L;
+      P.out_row0 = gslot * pl.Cpad;
       P.rowM = rowM;
       P.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0;
       if (launch_gemm<EPI_G, false, false>(KD_K_LOGITS_G, tmH_k, tmW_k, tmG_k, P, sms, st) != cudaSuccess)
@@ -349,6 +371,7 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       Q.kb_total = static_cast<int>(ceil_div(V, BK));
       Q.kb_per_split = pl.kbps_dh;
       Q.split_rows = pl.Cpad;
+      Q.a_mn0 = gslot * pl.Cpad;
       if (launch_gemm<EPI_F32, false, true>(KD_K_GEMM_DH, tmG_k, tmW_mn, tmDhp, Q, sms, st) != cudaSuccess)
         return KD_ERR_CUDA;
       {
@@ -361,16 +384,20 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
         prof_end(slot, st);
         if (e != cudaSuccess) return KD_ERR_CUDA;
       }
-      GemmParams R = base_params(status);  // dW (+)= G^T H, fp32
-      R.num_m = static_cast<int>(ceil_div(V, BM));
-      R.num_n = static_cast<int>(ceil_div(d, BN));
-      R.m_fast = 0;
-      R.kb_total = R.kb_per_split = pl.Cpad / BK;
-      R.b_k0 = static_cast<int>(t0);
-      R.reduce_add = (c == 0 && !accumulate) ? 0 : 1;  // first chunk stores, the rest add in L2
-      R.scale = dloss;
-      if (launch_gemm<EPI_F32, true, true>(KD_K_GEMM_DW, tmG_mn, tmH_mn, tmDW, R, sms, st) != cudaSuccess)
-        return KD_ERR_CUDA;
+      if (gslot == pl.dw_group - 1 || c == pl.nchunks - 1) {
+        // dW (+)= G^T H over the group's chunks, fp32; the first group stores, the rest add in L2
+        const int first = c - gslot;
+        GemmParams R = base_params(status);
+        R.num_m = static_cast<int>(ceil_div(V, BM));
+        R.num_n = static_cast<int>(ceil_div(d, BN));
+        R.m_fast = 0;
+        R.kb_total = R.kb_per_split = (gslot + 1) * pl.Cpad / BK;
+        R.b_k0 = static_cast<int>(int64_t(first) * pl.C);
+        R.reduce_add = (first == 0 && !accumulate) ? 0 : 1;
+        R.scale = dloss;
+        if (launch_gemm<EPI_F32, true, true>(KD_K_GEMM_DW, tmG_mn, tmH_mn, tmDW, R, sms, st) != cudaSuccess)
+          return KD_ERR_CUDA;
+      }
     }
   }
   return KD_OK;
