@@ -318,16 +318,53 @@ def run_kdtopk(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws)
     h2d = Hh.numel() * Hh.element_size() + ih.numel() * 4 + ph.numel() * 4
     peak_bytes = torch.cuda.max_memory_allocated(dev)
+    launches = sum(n for _, n in prof.values()) + prof["combine"][1]  # the loss reduction rides with combine
+
+    # ---- the same step without the backward recompute (kept exponentials -> G)
+    variants = {}
+    if not args.no_variants:
+        def step_nr():
+            api.fused_step_norecompute(H, W, idx, p, C, workspace=work, out=out, check=False)
+
+        for _ in range(args.warmup):
+            step_nr()
+        torch.cuda.synchronize(dev)
+        api.profile_enable(True)
+        api.profile_read(reset=True)
+        clocks_nr = ClockSampler(local)
+        clocks_nr.start()
+        time.sleep(0.3)
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step_nr()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        clk_nr = clocks_nr.stop()
+        prof_nr = api.profile_read(reset=True)
+        api.profile_enable(False)
+        N.check(api.device_status(work.buf, dev), "no-recompute steps")
+        ms_nr = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws)
+        variants["fused_norecompute"] = {
+            "value": ws * T / (ms_nr / 1e3), "unit": "tokens/s", "ms_per_step": ms_nr,
+            "tflops_actual_6TVd": ws * 6.0 * T * V * d / (ms_nr / 1e3) / 1e12,
+            "per_kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof_nr.items() if v[1]},
+            "launches_per_step": {k: v[1] // args.steps for k, v in prof_nr.items() if v[1]},
+            "clocks": clk_nr}
 
     nchunks = math.ceil(T / C)
     flops_8 = 8.0 * T * V * d
     flops_6 = 6.0 * T * V * d
     peaks = load_peaks()
-    # dominant kernel: the kind with the largest total time inside the timed region
+    # dominant kernel: the kind with the largest total time inside the timed region.
+    # Each chunk GEMM kind does 2 T V d flops per step in total; a dW launch covers
+    # a group of chunks, so per-launch work = 2 T V d / (its launches per step).
     gemm_kinds = ("logits_fwd", "logits_g", "gemm_dh", "gemm_dw")
     dom = max(prof, key=lambda k: prof[k][0])
     dom_ms, dom_n = prof[dom]
-    per_launch_flops = 2.0 * min(C, T) * V * d if dom in gemm_kinds else None
+    per_launch_flops = 2.0 * T * V * d / (dom_n / args.steps) if (dom in gemm_kinds and dom_n) else None
     achieved = per_launch_flops / (dom_ms / dom_n / 1e3) / 1e12 if per_launch_flops and dom_n else None
     traffic = None
     if (TRAFFIC["kernel"] == dom and TRAFFIC["workload"] == wl.name and C == get_workload(wl.name).chunk
@@ -336,6 +373,7 @@ def run_kdtopk(args):
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sustained"],
                 "unit": "TFLOP/s", "frac": (achieved / peaks["bf16_sustained"]) if achieved else None,
                 "traffic": traffic, "peak_kind": f"bf16 sustained ({peaks['source']})",
+                "flops_per_launch": per_launch_flops,
                 "frac_of_burst_peak": (achieved / peaks["bf16"]) if achieved else None,
                 "per_kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
                 "launches_per_step": {k: v[1] // args.steps for k, v in prof.items() if v[1]}}
@@ -362,8 +400,9 @@ def run_kdtopk(args):
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": 4},
-            "gpu_launches": 8 * nchunks * args.steps,
+            "gpu_launches": launches,
             "clocks": clk,
+            "variants": variants,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -421,6 +460,53 @@ def run_sweep(args):
     return 0
 
 
+def run_topk_cache(args):
+    """Teacher-cache builder: top-K ids and probabilities of every row of
+    synthetic teacher logits Z [T, V] (bf16), one JSON line.  HBM-bound: the
+    algorithmic bytes are one read of Z plus the cache written (idx, p, lse)."""
+    import torch
+
+    from lm_head_top_tma_b300 import api
+    from lm_head_top_tma_b300.inputs import make_teacher_logits
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    T, V, K = args.T or 32768, 128256, 100
+    Z = make_teacher_logits(T, V, seed=7, device=dev, dtype="bf16")
+    for _ in range(max(3, args.warmup)):
+        api.topk_cache_build(Z, K)
+    torch.cuda.synchronize(dev)
+    api.profile_enable(True)
+    api.profile_read(reset=True)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        api.topk_cache_build(Z, K)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    prof = api.profile_read(reset=True)
+    api.profile_enable(False)
+    ms = e0.elapsed_time(e1) / args.steps
+    kern_ms, kern_n = prof["other"]
+    bytes_alg = T * V * 2 + T * K * 8 + T * 4
+    peaks = load_peaks()
+    achieved = bytes_alg / (kern_ms / kern_n / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "teacher top-K cache build rows/s", "value": T / (ms / 1e3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic", "config": {"workload": "teacher_logits", "T": T, "V": V, "K": K,
+                                                          "l2": "logits larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm"], "traffic": None, "bytes_per_launch": bytes_alg},
+        "clocks": clk}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,10 +517,14 @@ def main():
     ap.add_argument("--T", type=int, default=None, help="override the sequence length (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true", help="skip the no-recompute fused step timing")
     ap.add_argument("--sweep", action="store_true", help="output-head-only T sweep, one line per T")
+    ap.add_argument("--topk-cache", action="store_true", help="teacher-cache builder over synthetic logits")
     args = ap.parse_args()
     if args.sweep:
         return run_sweep(args)
+    if args.topk_cache:
+        return run_topk_cache(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_kdtopk(args)

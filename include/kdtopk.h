@@ -129,6 +129,26 @@ KD_API kd_status kd_topk_kl_fused_step(const void* H, const void* W, const int32
                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The same forward and backward in one pass over the chunks, without the
+ * backward's second logits GEMM: the forward GEMM's epilogue also writes the
+ * chunk's exponentials e_tj = exp(z_tj - m_t,tile) (rounded to bf16, one
+ * [chunk, V] buffer that the workspace already holds for G), and once lse_t is
+ * known an elementwise pass forms G_tj = M_t e_tj exp(m_t,tile - lse_t) -
+ * (p at the ids) in place, rounded to bf16 once.  Three chunk GEMMs instead of
+ * four (6 T V d instead of 8 T V d flops); the logits still never exist for
+ * more than one chunk (or one dW group of chunks), so the workspace is the
+ * fused step's, flat in T.  This trades the recompute the paper's fused loss
+ * performs (thorstenmeyerai.com pipeline step "Recompute backward") for one
+ * extra bf16 rounding of G (relative 2^-9).  Arguments, outputs, ownership and
+ * errors as kd_topk_kl_fused_step; workspace size: KD_WS_FUSED.
+ */
+KD_API kd_status kd_topk_kl_fused_step_norecompute(const void* H, const void* W, const int32_t* idx,
+                                            const float* p, int64_t T, int d, int V, int K, int chunk,
+                                            float dloss, float* loss, float* lse, float* loss_rows,
+                                            float* dH, float* dW, int accumulate_dW,
+                                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * kd_topk_kl_forward for callers that cannot allocate device memory (the
  * paper has no counterpart; this is a convenience of this library).  Same
  * inputs, outputs and results as kd_topk_kl_forward, but the workspace is a
@@ -157,6 +177,24 @@ KD_API kd_status kd_topk_kl_forward_noalloc(const void* H, const void* W, const 
                                             float* loss, float* lse, float* loss_rows, void* stream);
 
 /*
+ * Teacher-cache builder: the offline step that turns teacher logits into the
+ * top-K cache this loss consumes (thorstenmeyerai.com pipeline, "Infer once"
+ * and "Select top-K"; aimodeling.com "First cut": the top-100 probabilities
+ * of every token are cached).  For each row t of logits[T, V] (row-major,
+ * device memory; bf16 if logits_bf16 != 0, else fp32; 2- or 4-byte aligned):
+ *   idx[t, 0..K)  the ids of the K largest logits, largest first, equal
+ *                 logits ordered by ascending id (int32, device, [T, K]);
+ *   p[t, k]       exp(z_t,idx - lse_t), the teacher's softmax probability
+ *                 (fp32, device, [T, K]); the row mass sum_k p <= 1;
+ *   lse[t]        log sum_j exp(z_tj) (fp32, device, [T]; may be NULL).
+ * Temperature 1.  -inf logits carry no probability.  1 <= K <= min(V, 1024)
+ * (KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED otherwise).  Allocates nothing,
+ * asynchronous on `stream`; no device-side errors are possible.
+ */
+KD_API kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, int V, int K,
+                                     int32_t* idx, float* p, float* lse, void* stream);
+
+/*
  * Waits for `stream`, then returns and clears the device-side status the
  * last call on this workspace recorded (KD_OK, KD_ERR_BAD_INDEX or
  * KD_ERR_TIMEOUT), or KD_ERR_CUDA if the wait itself failed.
@@ -171,11 +209,13 @@ KD_API const char* kd_status_string(kd_status s);
  * D[M,N] (fp32, row stride ldd elements) = A B^T with bf16 A and B.
  * a_mn == 0: A is stored [M,K] row-major (row stride lda); a_mn == 1: A is
  * stored [K,M] row-major.  Likewise b_mn for B ([N,K] or [K,N], stride ldb).
- * Strides are in elements and must give 16-byte-aligned rows.  `workspace`
- * (>= 256 bytes) holds the status word read by kd_topk_kl_device_status.
+ * Strides are in elements and must give 16-byte-aligned rows.  cta_pair != 0
+ * runs the two-CTA-cluster form (256-row tiles, cta_group::2 MMAs) that the
+ * loss uses for chunks of 256 rows or more.  `workspace` (>= 256 bytes) holds
+ * the status word read by kd_topk_kl_device_status.
  */
 KD_API kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int K,
-                       int lda, int ldb, int ldd, int a_mn, int b_mn,
+                       int lda, int ldb, int ldd, int a_mn, int b_mn, int cta_pair,
                        void* workspace, size_t ws_bytes, void* stream);
 
 /*
@@ -183,10 +223,12 @@ KD_API kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int
  * withheld, so the first internal wait runs out after `wait_limit_ms`; the
  * kernel then winds down (frees tensor memory, returns) and records
  * KD_ERR_TIMEOUT in the workspace (>= 256 bytes), which this call returns
- * after synchronising `stream`.  No fault, trap or hang is involved; the
+ * after synchronising `stream`.  cta_pair != 0 runs it on one two-CTA
+ * cluster (both CTAs wind down).  No fault, trap or hang is involved; the
  * context stays usable.
  */
-KD_API kd_status kd_debug_wait_timeout(int wait_limit_ms, void* workspace, size_t ws_bytes, void* stream);
+KD_API kd_status kd_debug_wait_timeout(int wait_limit_ms, int cta_pair, void* workspace, size_t ws_bytes,
+                                      void* stream);
 
 /*
  * Optional per-kernel timing (CUDA events recorded on the launching stream
@@ -194,9 +236,10 @@ KD_API kd_status kd_debug_wait_timeout(int wait_limit_ms, void* workspace, size_
  * kd_profile_read synchronises, fills per-kind totals and launch counts for
  * up to `n` kinds and returns the number of kinds (KD_PROF_KINDS).
  */
-#define KD_PROF_KINDS 8
+#define KD_PROF_KINDS 9
 enum { KD_K_PREP = 0, KD_K_LOGITS_FWD = 1, KD_K_COMBINE = 2, KD_K_LOGITS_G = 3,
-       KD_K_GEMM_DH = 4, KD_K_DH_REDUCE = 5, KD_K_GEMM_DW = 6, KD_K_OTHER = 7 };
+       KD_K_GEMM_DH = 4, KD_K_DH_REDUCE = 5, KD_K_GEMM_DW = 6, KD_K_OTHER = 7,
+       KD_K_G_FROM_E = 8 };
 KD_API kd_status kd_profile_enable(int on);
 KD_API int kd_profile_read(double* ms_total, int64_t* launches, int n, int reset);
 KD_API const char* kd_profile_kind_name(int kind);

@@ -22,7 +22,7 @@ KD_WS_FORWARD = 1
 KD_WS_BACKWARD = 2
 KD_WS_FUSED = 3
 
-KD_PROF_KINDS = 8
+KD_PROF_KINDS = 9
 KD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _c_p = ctypes.c_void_p
@@ -40,13 +40,16 @@ SIGNATURES = {
                                    _f32, _c_p, _c_p, _i32, _c_p, _sz, _c_p]),
     "kd_topk_kl_fused_step": (_i32, [_c_p, _c_p, _c_p, _c_p, _i64, _i32, _i32, _i32, _i32,
                                      _f32, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _c_p, _sz, _c_p]),
+    "kd_topk_kl_fused_step_norecompute": (_i32, [_c_p, _c_p, _c_p, _c_p, _i64, _i32, _i32, _i32, _i32,
+                                                 _f32, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _c_p, _sz, _c_p]),
+    "kd_topk_cache_build": (_i32, [_c_p, _i32, _i64, _i32, _i32, _c_p, _c_p, _c_p, _c_p]),
     "kd_topk_kl_device_status": (_i32, [_c_p, _c_p]),
     "kd_topk_kl_forward_noalloc": (_i32, [_c_p, _c_p, _c_p, _c_p, _i64, _i32, _i32, _i32, _i32,
                                           _c_p, _c_p, _c_p, _c_p]),
     "kd_status_string": (ctypes.c_char_p, [_i32]),
-    "kd_gemm_bf16": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+    "kd_gemm_bf16": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                             _c_p, _sz, _c_p]),
-    "kd_debug_wait_timeout": (_i32, [_i32, _c_p, _sz, _c_p]),
+    "kd_debug_wait_timeout": (_i32, [_i32, _i32, _c_p, _sz, _c_p]),
     "kd_profile_enable": (_i32, [_i32]),
     "kd_profile_read": (_i32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), _i32, _i32]),
     "kd_profile_kind_name": (ctypes.c_char_p, [_i32]),

@@ -13,6 +13,7 @@ import torch
 from . import _native as N
 
 __all__ = ["workspace_size", "Workspace", "forward", "forward_noalloc", "backward", "fused_step",
+           "fused_step_norecompute", "topk_cache_build",
            "device_status", "gemm_bf16", "debug_wait_timeout", "TopKKLLoss",
            "profile_enable", "profile_read"]
 
@@ -149,6 +150,20 @@ def fused_step(H, W, idx, p, chunk: int, *, dloss: float = 1.0, dW: torch.Tensor
                check: bool = True, out: dict | None = None):
     """Forward + backward in one chunk loop.  Returns a dict with loss, lse,
     dH, dW (and loss_rows).  ``out`` may supply preallocated outputs."""
+    return _fused(N.load().kd_topk_kl_fused_step, "kd_topk_kl_fused_step", H, W, idx, p, chunk, dloss, dW,
+                  accumulate_dW, loss_rows, workspace, check, out)
+
+
+def fused_step_norecompute(H, W, idx, p, chunk: int, *, dloss: float = 1.0, dW: torch.Tensor | None = None,
+                           accumulate_dW: bool = False, loss_rows: bool = False,
+                           workspace: Workspace | None = None, check: bool = True, out: dict | None = None):
+    """``fused_step`` without the backward's second logits GEMM: G is formed
+    elementwise from the exponentials the forward GEMM kept (same workspace)."""
+    return _fused(N.load().kd_topk_kl_fused_step_norecompute, "kd_topk_kl_fused_step_norecompute", H, W, idx,
+                  p, chunk, dloss, dW, accumulate_dW, loss_rows, workspace, check, out)
+
+
+def _fused(fn, name, H, W, idx, p, chunk, dloss, dW, accumulate_dW, loss_rows, workspace, check, out):
     dev, T, d, V, K = _inputs(H, W, idx, p)
     ws_n = workspace_size(T, d, V, K, chunk, "fused")
     ws = (workspace or Workspace(dev)).get(ws_n)
@@ -161,33 +176,52 @@ def fused_step(H, W, idx, p, chunk: int, *, dloss: float = 1.0, dW: torch.Tensor
     lrows = None
     if loss_rows:
         lrows = o.get("loss_rows") if o.get("loss_rows") is not None else torch.empty(T, dtype=torch.float32, device=dev)
-    rc = N.load().kd_topk_kl_fused_step(_ptr(H), _ptr(W), _ptr(idx), _ptr(p), T, d, V, K, int(chunk),
-                                        float(dloss), _ptr(loss), _ptr(lse), _ptr(lrows), _ptr(dH), _ptr(dW),
-                                        int(bool(accumulate_dW)), _ptr(ws), ws.numel(), _stream(dev))
-    N.check(rc, "kd_topk_kl_fused_step")
-    _finish(ws, dev, "kd_topk_kl_fused_step", check)
+    rc = fn(_ptr(H), _ptr(W), _ptr(idx), _ptr(p), T, d, V, K, int(chunk), float(dloss), _ptr(loss), _ptr(lse),
+            _ptr(lrows), _ptr(dH), _ptr(dW), int(bool(accumulate_dW)), _ptr(ws), ws.numel(), _stream(dev))
+    N.check(rc, name)
+    _finish(ws, dev, name, check)
     res = {"loss": loss, "lse": lse, "dH": dH, "dW": dW}
     if loss_rows:
         res["loss_rows"] = lrows
     return res
 
 
-def gemm_bf16(A, B, M, N_, K, *, a_mn=False, b_mn=False, out=None, check=True):
-    """D = A B^T on the library's tcgen05 GEMM (A [M,K] or [K,M]; B [N,K] or [K,N])."""
+def topk_cache_build(Z, K: int, *, lse: bool = True):
+    """Teacher cache from logits Z [T,V] (bf16 or fp32, CUDA): ids of the K
+    largest logits (largest first, ties by ascending id), their softmax
+    probabilities, and lse.  Returns (idx int32 [T,K], p fp32 [T,K], lse fp32 [T] or None)."""
+    if not isinstance(Z, torch.Tensor) or not Z.is_cuda or Z.dim() != 2 or not Z.is_contiguous():
+        raise ValueError("Z must be a contiguous 2-D CUDA tensor")
+    if Z.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("Z must be bf16 or fp32")
+    T, V = Z.shape
+    dev = Z.device
+    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    p = torch.empty(T, K, dtype=torch.float32, device=dev)
+    l = torch.empty(T, dtype=torch.float32, device=dev) if lse else None
+    rc = N.load().kd_topk_cache_build(_ptr(Z), int(Z.dtype == torch.bfloat16), T, V, int(K), _ptr(idx), _ptr(p),
+                                      _ptr(l), _stream(dev))
+    N.check(rc, "kd_topk_cache_build")
+    return idx, p, l
+
+
+def gemm_bf16(A, B, M, N_, K, *, a_mn=False, b_mn=False, cta_pair=False, out=None, check=True):
+    """D = A B^T on the library's tcgen05 GEMM (A [M,K] or [K,M]; B [N,K] or [K,N]);
+    ``cta_pair`` selects the two-CTA-cluster form."""
     dev = A.device
     D = out if out is not None else torch.empty(M, N_, dtype=torch.float32, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
     rc = N.load().kd_gemm_bf16(_ptr(A), _ptr(B), _ptr(D), M, N_, K, A.stride(0), B.stride(0), D.stride(0),
-                               int(a_mn), int(b_mn), _ptr(ws), ws.numel(), _stream(dev))
+                               int(a_mn), int(b_mn), int(bool(cta_pair)), _ptr(ws), ws.numel(), _stream(dev))
     N.check(rc, "kd_gemm_bf16")
     _finish(ws, dev, "kd_gemm_bf16", check)
     return D
 
 
-def debug_wait_timeout(limit_ms: int, device=None) -> int:
+def debug_wait_timeout(limit_ms: int, device=None, cta_pair: bool = False) -> int:
     dev = torch.device(device or "cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    return N.load().kd_debug_wait_timeout(int(limit_ms), _ptr(ws), ws.numel(), _stream(dev))
+    return N.load().kd_debug_wait_timeout(int(limit_ms), int(bool(cta_pair)), _ptr(ws), ws.numel(), _stream(dev))
 
 
 def profile_enable(on: bool = True):

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkdtopk.so")
 SOURCES = ["kdtopk.cu"]
-DEPS = ["kdtopk.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh"]
+DEPS = ["kdtopk.cu", "kd_gemm.cuh", "kd_aux.cuh", "kd_ptx.cuh", "kd_cache.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -4,9 +4,13 @@
 //            plus the id range check;
 //   combine  per-(row, vocabulary tile) softmax partials -> lse_t and the
 //            per-row loss L_t = E_t - sum_k p_tk z_tk + M_t lse_t;
-//   reductions of the loss (fp64, fixed order) and of split-K dH partials.
+//   reductions of the loss (fp64, fixed order) and of split-K dH partials;
+//   g_from_e the gradient operand G = M_t softmax(z_t) - p at the ids, formed
+//            in place from the exponentials the forward GEMM kept (the fused
+//            step without the backward recompute).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -179,6 +183,87 @@ __global__ void kd_dh_reduce_kernel(const float4* __restrict__ part, int S, int6
     a.z *= scale;
     a.w *= scale;
     dH[i] = a;
+  }
+}
+
+constexpr int GPASS_THREADS = 256;
+constexpr int GPASS_VEC = 8;     // bf16 per 16-byte access
+constexpr int GPASS_UNROLL = 4;  // accesses in flight per thread
+constexpr int GPASS_TILE = 256;  // vocabulary tile of the partials
+constexpr int GPASS_MAXK = 1024;
+
+// In place over the rows of the chunk's operand buffer:
+//   G[r, j] = bf16( M_r * e[r, j] * 2^(m[r, j / 256] - lse_r log2 e) - sum_{k: id_rk = j} p_rk )
+// where e = 2^(z log2 e - m) was rounded to bf16 by the forward GEMM and m is
+// that tile's base-2 row maximum (the softmax partials).  The teacher
+// correction is subtracted in fp32 before the single rounding.  Columns in
+// [V, ldg) are set to 0.  One block per row (rows r = blockIdx.x, + gridDim.x,
+// ...): thread t visits 16-byte groups t, t + 256, ... in increasing column
+// order, so a per-thread cursor over the row's sorted ids (staged in shared
+// memory) finds the corrections of each group.
+__global__ void __launch_bounds__(GPASS_THREADS)
+    kd_g_from_e_kernel(__nv_bfloat16* __restrict__ G, int64_t ldg, int rows, int V, int K,
+                       const int32_t* __restrict__ sidx, const float* __restrict__ sp,
+                       const float* __restrict__ rowM, const float* __restrict__ lse,
+                       const float* __restrict__ part_m, int ld_part) {
+  __shared__ int s_id[GPASS_MAXK + 1];
+  __shared__ float s_p[GPASS_MAXK];
+  const int ngroups = static_cast<int>(ldg / GPASS_VEC);
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    __syncthreads();  // the previous row's ids are no longer read
+    for (int k = threadIdx.x; k < K; k += GPASS_THREADS) {
+      s_id[k] = __ldg(sidx + static_cast<size_t>(r) * K + k);
+      s_p[k] = __ldg(sp + static_cast<size_t>(r) * K + k);
+    }
+    if (threadIdx.x == 0) s_id[K] = INT_MAX;  // sentinel
+    __syncthreads();
+    const float Mr = __ldg(rowM + r);
+    const float nl2 = -__ldg(lse + r) * kLog2e;
+    const float* pmr = part_m + r;
+    __nv_bfloat16* grow = G + static_cast<size_t>(r) * ldg;
+    int cur = 0;  // first sorted id not below this thread's next group
+    for (int g0 = threadIdx.x; g0 < ngroups; g0 += GPASS_THREADS * GPASS_UNROLL) {
+      uint4 raw[GPASS_UNROLL];
+      float scale[GPASS_UNROLL];
+#pragma unroll
+      for (int u = 0; u < GPASS_UNROLL; ++u) {
+        const int g = g0 + u * GPASS_THREADS;
+        if (g < ngroups) {
+          raw[u] = *reinterpret_cast<const uint4*>(grow + static_cast<size_t>(g) * GPASS_VEC);
+          scale[u] = __ldg(pmr + static_cast<size_t>(g * GPASS_VEC / GPASS_TILE) * ld_part);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < GPASS_UNROLL; ++u) {
+        const int g = g0 + u * GPASS_THREADS;
+        if (g >= ngroups) break;
+        const int col = g * GPASS_VEC;
+        const float sc = Mr * ex2(scale[u] + nl2);
+        const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+        float v[GPASS_VEC];
+#pragma unroll
+        for (int j = 0; j < GPASS_VEC / 2; ++j) {
+          const float2 f = __bfloat1622float2(e2[j]);
+          v[2 * j] = f.x * sc;
+          v[2 * j + 1] = f.y * sc;
+        }
+        while (s_id[cur] < col) ++cur;
+        for (int k = cur; s_id[k] < col + GPASS_VEC; ++k) {
+          const int off = s_id[k] - col;
+          const float pv = s_p[k];
+#pragma unroll
+          for (int j = 0; j < GPASS_VEC; ++j) v[j] = (j == off) ? v[j] - pv : v[j];
+        }
+#pragma unroll
+        for (int j = 0; j < GPASS_VEC; ++j)
+          if (col + j >= V) v[j] = 0.f;
+        uint4 outv;
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&outv);
+#pragma unroll
+        for (int j = 0; j < GPASS_VEC / 2; ++j) o2[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+        *reinterpret_cast<uint4*>(grow + col) = outv;
+      }
+    }
   }
 }
 

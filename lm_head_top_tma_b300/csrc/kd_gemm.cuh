@@ -1,12 +1,24 @@
 // Persistent, warp-specialised tcgen05 GEMM for sm_103a:  D[M,N] = A[M,K] B[N,K]^T
-// with bf16 operands staged by TMA (128-byte swizzle) into a 4-deep shared-memory
-// ring and fp32 accumulators double-buffered in tensor memory (2 x 256 columns).
+// with bf16 operands staged by TMA (128-byte swizzle) into a shared-memory ring
+// and fp32 accumulators double-buffered in tensor memory (2 x 256 columns).
 //
 //   warp 0      TMA producer (one thread)
 //   warp 1      tensor-memory allocator and MMA issuer (one thread)
 //   warps 2..5  epilogue: thread i of the four warps owns accumulator row i
 //
-// Tile 128 x 256 x 64.  Operands may be K-major (the reduction index is
+// Two forms, chosen by the PAIR template parameter:
+//   single CTA  tile 128 x 256 x 64, 4-stage ring of 48 KB stages;
+//   CTA pair    a two-CTA cluster computes a 256 x 256 tile with cta_group::2
+//               MMAs issued by the leader CTA: each CTA stages its own 128 rows
+//               of A and its own 128 rows of B (32 KB stages, 6-stage ring),
+//               the MMA reads B from both CTAs, and each CTA's tensor memory
+//               holds its 128 rows of D.  Per MMA flop the pair moves a third
+//               less operand data from L2 into shared memory.  The peer's TMA
+//               loads signal the leader's "full" barriers; MMA completion is
+//               multicast to both CTAs' "empty" / "accumulator full" barriers;
+//               the peer's epilogue releases accumulators to the leader.
+//
+// Tile 128 x 256 x 64 per CTA.  Operands may be K-major (the reduction index is
 // contiguous in memory) or MN-major (the row/column index is contiguous); the
 // latter lets the backward GEMMs read W, G and H in place.
 //
@@ -19,6 +31,11 @@
 //            rounded to bf16, staged as 128 x 64 swizzled slices and written
 //            by TMA as the [chunk, V] operand of dH / dW (TMA clips the
 //            vocabulary tail).
+//   EPI_FWD_E  as EPI_FWD, and the tile's exponentials e = 2^(z log2e - m) with
+//            m the tile's row maximum are kept: rounded to bf16 and written by
+//            TMA into the chunk's [chunk, V] operand buffer, where a later
+//            elementwise pass turns them into G once lse is known (the fused
+//            step without the backward recompute).
 //   EPI_F32  fp32 tile, scaled, staged through shared memory (128 x 32 slices,
 //            128-byte swizzle) and written by TMA: a plain store, or a TMA
 //            reduce-add so that L2 performs the read-modify-write of dW while
@@ -49,12 +66,26 @@ constexpr int OUT_STAGING_BYTES = 2 * OUT_SLICE_BYTES;
 constexpr int EPI_WARPS = 4;
 constexpr uint32_t EPI_BAR_ID = 1;  // named barrier of the epilogue warps
 
-enum Epi { EPI_FWD = 0, EPI_G = 1, EPI_F32 = 2 };
+enum Epi { EPI_FWD = 0, EPI_G = 1, EPI_F32 = 2, EPI_FWD_E = 3 };
 
 __host__ __device__ constexpr int staging_bytes(int epi) { return epi == EPI_FWD ? 0 : OUT_STAGING_BYTES; }
+
+// Per-form shape of the pipeline.
+template <bool PAIR>
+struct GemmCfg {
+  static constexpr int NCTA = PAIR ? 2 : 1;
+  static constexpr int TILE_M = BM * NCTA;                  // rows of D per tile
+  static constexpr int B_ROWS = BN / NCTA;                  // rows of the B tile one CTA stages
+  static constexpr int STAGE = A_STAGE_BYTES + B_ROWS * BK * 2;
+  static constexpr int NSTAGE = PAIR ? 6 : STAGES;
+};
+
+template <bool PAIR>
 __host__ __device__ constexpr size_t gemm_smem_bytes(int epi) {
-  return 1024 + size_t(STAGES) * STAGE_BYTES + staging_bytes(epi) + SMEM_BAR_BYTES;
+  return 1024 + size_t(GemmCfg<PAIR>::NSTAGE) * GemmCfg<PAIR>::STAGE + staging_bytes(epi) + SMEM_BAR_BYTES;
 }
+static_assert(gemm_smem_bytes<true>(EPI_F32) <= 232448, "pair pipeline exceeds the shared-memory limit");
+static_assert(gemm_smem_bytes<false>(EPI_F32) <= 232448, "pipeline exceeds the shared-memory limit");
 
 struct GemmParams {
   // tile grid and raster
@@ -104,34 +135,67 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+// One 32-column window of this thread's accumulator row, rounded to bf16, into
+// the 128 x 64 staging slice `buf` (128-byte rows, 16-byte chunks swizzled by
+// row % 8); window c fills the left (c even) or right (c odd) half.
+__device__ __forceinline__ void stage_bf16_window(uint32_t buf, int row_in_tile, int c, const float (&g)[32]) {
+  const uint32_t row_addr = buf + row_in_tile * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t chunk = static_cast<uint32_t>(((c & 1) << 2) + j) ^ static_cast<uint32_t>(row_in_tile & 7);
+    st_shared_v4_b32(row_addr + (chunk << 4), pack_bf16x2(g[8 * j + 0], g[8 * j + 1]),
+                     pack_bf16x2(g[8 * j + 2], g[8 * j + 3]), pack_bf16x2(g[8 * j + 4], g[8 * j + 5]),
+                     pack_bf16x2(g[8 * j + 6], g[8 * j + 7]));
+  }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
+  if constexpr (PAIR) tma_load_2d_pair(dst, tm, x, y, bar);
+  else tma_load_2d(dst, tm, x, y, bar);
+}
+
+// MMA completion -> mbarrier at offset `bar`: this CTA's (single form) or both
+// CTAs' of the pair (mask 0b11), or the leader's only (mask 0b01).
+template <bool PAIR>
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t pair_mask) {
+  if constexpr (PAIR) umma_commit_pair_mc(bar, pair_mask);
+  else umma_commit(bar);
+}
+
+template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const GemmParams P) {
+  using Cfg = GemmCfg<PAIR>;
+  constexpr int NST = Cfg::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint8_t* staging = smem + NST * Cfg::STAGE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + staging_bytes(EPI));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NST + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA rank within the pair (0 = leader: issues the MMAs, owns D rows 0-127 of each tile)
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
   // barrier map: full[s], empty[s], tmem_full[2], tmem_empty[2], drain
-  const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES;
-  const uint32_t tfull0 = bar0 + 16u * STAGES, tempty0 = tfull0 + 16u;
+  const uint32_t full0 = bar0, empty0 = bar0 + 8u * NST;
+  const uint32_t tfull0 = bar0 + 16u * NST, tempty0 = tfull0 + 16u;
   const uint32_t drain_bar = tempty0 + 16u;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8u * a, 1);
-      mbar_init(tempty0 + 8u * a, 4);
+      mbar_init(tempty0 + 8u * a, EPI_WARPS * Cfg::NCTA);  // both CTAs' epilogue warps release
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -143,16 +207,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if constexpr (EPI != EPI_FWD) prefetch_tmap(&tmD);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<PAIR>(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish<PAIR>();
     tc_fence_before();
   }
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before anything signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtl wc{P.wait_limit_ns, abort_flag, P.status, KD_ERR_TIMEOUT};
   const int num_tiles = P.num_m * P.num_n * P.num_s;
+  const int tile0 = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int tile_step = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -160,57 +227,68 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
         int m, n, s;
         decode_tile(P, tile, m, n, s);
         const int kb0 = s * P.kb_per_split;
         const int kb1 = min(P.kb_total, kb0 + P.kb_per_split);
+        const int a_row = P.a_mn0 + m * Cfg::TILE_M + static_cast<int>(rank) * BM;
+        const int b_row = P.b_mn0 + n * BN + static_cast<int>(rank) * Cfg::B_ROWS;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wc)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full0 + 8u * stage;
-          const uint32_t a_dst = smem_base + stage * STAGE_BYTES;
+          const uint32_t fb_local = full0 + 8u * stage;
+          // the pair's loads all complete on the leader's barrier
+          const uint32_t fb = PAIR ? mapa_shared(fb_local, 0) : fb_local;
+          const uint32_t a_dst = smem_base + stage * Cfg::STAGE;
           const uint32_t b_dst = a_dst + A_STAGE_BYTES;
           if (!P.debug_withhold_loads) {
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            armed |= 1u << stage;
-            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            if (leader) {
+              mbar_arrive_expect_tx(fb_local, Cfg::NCTA * Cfg::STAGE);
+              armed |= 1u << stage;
+              armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            }
             if (!A_MN) {
-              tma_load_2d(a_dst, &tmA, P.a_k0 + kb * BK, P.a_mn0 + m * BM, fb);
+              load_tile<PAIR>(a_dst, &tmA, P.a_k0 + kb * BK, a_row, fb);
             } else {
 #pragma unroll
               for (int j = 0; j < BM / 64; ++j)
-                tma_load_2d(a_dst + j * 8192, &tmA, P.a_mn0 + m * BM + j * 64, P.a_k0 + kb * BK, fb);
+                load_tile<PAIR>(a_dst + j * 8192, &tmA, a_row + j * 64, P.a_k0 + kb * BK, fb);
             }
             if (!B_MN) {
-              tma_load_2d(b_dst, &tmB, P.b_k0 + kb * BK, P.b_mn0 + n * BN, fb);
+              load_tile<PAIR>(b_dst, &tmB, P.b_k0 + kb * BK, b_row, fb);
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(b_dst + j * 8192, &tmB, P.b_mn0 + n * BN + j * 64, P.b_k0 + kb * BK, fb);
+              for (int j = 0; j < Cfg::B_ROWS / 64; ++j)
+                load_tile<PAIR>(b_dst + j * 8192, &tmB, b_row + j * 64, P.b_k0 + kb * BK, fb);
             }
           }
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) {  // let copies already in flight land before the CTA exits
-        for (int s2 = 0; s2 < STAGES; ++s2)
+        for (int s2 = 0; s2 < NST; ++s2)
           if ((armed >> s2) & 1u) mbar_wait_quiet(full0 + 8u * s2, (armed_par >> s2) & 1u, P.wait_limit_ns);
+        if constexpr (PAIR) {  // the peer cannot observe its own loads: give them time to land
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    // ------------------------------------------------------------ MMA issuer (the leader's, for a pair)
+    if (lane == 0 && leader) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(Cfg::TILE_M, BN, A_MN, B_MN);
       int stage = 0, local = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+      for (int tile = tile0; tile < num_tiles && ok; tile += tile_step, ++local) {
         int m, n, s;
         decode_tile(P, tile, m, n, s);
         const int kb0 = s * P.kb_per_split;
@@ -226,7 +304,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_base + stage * STAGE_BYTES;
+          const uint32_t a_base = smem_base + stage * Cfg::STAGE;
           const uint32_t b_base = a_base + A_STAGE_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
@@ -234,19 +312,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                      : sdesc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b_base + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(b_base + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+            if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, IDESC, accum);
+            else umma_bf16(d_tmem, ad, bd, IDESC, accum);
           }
-          umma_commit(empty0 + 8u * stage);  // frees the stage once these MMAs finish
-          if (++stage == STAGES) {
+          mma_commit<PAIR>(empty0 + 8u * stage, 0x3);  // frees the stage (in both CTAs) once these MMAs finish
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(tfull0 + 8u * acc);  // accumulator ready for the epilogue
+        mma_commit<PAIR>(tfull0 + 8u * acc, 0x3);  // accumulator ready for the epilogue(s)
       }
       // every MMA issued above must be complete before tensor memory is freed
-      umma_commit(drain_bar);
+      mma_commit<PAIR>(drain_bar, 0x1);
       mbar_wait_quiet(drain_bar, 0, P.wait_limit_ns);
     }
   } else {
@@ -257,13 +337,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t staging_base = smem_u32(staging);
     uint32_t slice = 0;  // running count of output slices (alternates staging buffers)
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = tile0; tile < num_tiles; tile += tile_step, ++local) {
       int m, n, s;
       decode_tile(P, tile, m, n, s);
       const int acc = local & 1;
       const uint32_t acc_par = (local >> 1) & 1;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      const int r = m * BM + row_in_tile;
+      const int row0 = m * Cfg::TILE_M + static_cast<int>(rank) * BM;  // first row of D this CTA holds
+      const int r = row0 + row_in_tile;
 
       // per-row set-up, overlapping the mainloop of this tile
       const int32_t* ids = nullptr;
@@ -271,7 +352,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int cur = 0, cid = INT_MAX;
       float cp = 0.f, Mr = 0.f, nl2 = 0.f;
       bool rv = false;
-      if constexpr (EPI == EPI_FWD || EPI == EPI_G) {
+      if constexpr (EPI == EPI_FWD || EPI == EPI_G || EPI == EPI_FWD_E) {
         rv = r < P.rows_valid;
         const int n0 = n * BN;
         ids = P.sidx + static_cast<size_t>(r) * P.K;
@@ -304,6 +385,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
 
       float run_m = -INFINITY, run_s = 0.f, pz = 0.f;
+      if constexpr (EPI == EPI_FWD_E) {
+        // first pass over the accumulator: the row's maximum over the tile's
+        // vocabulary columns, the reference point of the kept exponentials
+        float tmax = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int nv = P.V - (n * BN + c * 32);  // <= 0 past the vocabulary
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv) tmax = fmaxf(tmax, v[j]);
+        }
+        run_m = tmax * kLog2e;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         float v[32];
@@ -356,19 +452,55 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             cid = cur < P.K ? __ldg(ids + cur) : INT_MAX;
             cp = cur < P.K ? __ldg(ps + cur) : 0.f;
           }
-          const uint32_t row_addr = buf + row_in_tile * 128;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {  // 16-byte chunk (c & 1) * 4 + j of the row, swizzled
-            const uint32_t chunk = static_cast<uint32_t>(((c & 1) << 2) + j) ^ static_cast<uint32_t>(row_in_tile & 7);
-            st_shared_v4_b32(row_addr + (chunk << 4), pack_bf16x2(g[8 * j + 0], g[8 * j + 1]),
-                             pack_bf16x2(g[8 * j + 2], g[8 * j + 3]), pack_bf16x2(g[8 * j + 4], g[8 * j + 5]),
-                             pack_bf16x2(g[8 * j + 6], g[8 * j + 7]));
-          }
+          stage_bf16_window(buf, row_in_tile, c, g);
           if (c & 1) {
             fence_proxy_async_smem();
             named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
             if (out_leader) {
-              tma_store_2d(&tmD, n * BN + (c >> 1) * G_SLICE_COLS, P.out_row0 + m * BM, buf);
+              tma_store_2d(&tmD, n * BN + (c >> 1) * G_SLICE_COLS, P.out_row0 + row0, buf);
+              bulk_commit();
+            }
+            ++slice;
+          }
+        } else if constexpr (EPI == EPI_FWD_E) {
+          const uint32_t buf = staging_base + (slice & 1u) * OUT_SLICE_BYTES;
+          if ((c & 1) == 0) {
+            if (out_leader) bulk_wait_read1();  // the store that last read `buf` is done with it
+            named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
+          }
+          const int nv = P.V - col0;  // <= 0 past the vocabulary
+          float e[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) e[j] = (j < nv) ? ex2(fmaf(v[j], kLog2e, -run_m)) : 0.f;
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            s0 += e[j];
+            s1 += e[j + 1];
+            s2 += e[j + 2];
+            s3 += e[j + 3];
+          }
+          run_s += (s0 + s1) + (s2 + s3);
+          while (cid < col0 + 32) {
+            const int off = cid - col0;
+            float sel = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sel = (j == off) ? v[j] : sel;
+            pz = fmaf(cp, sel, pz);
+            ++cur;
+            cid = cur < P.K ? __ldg(ids + cur) : INT_MAX;
+            cp = cur < P.K ? __ldg(ps + cur) : 0.f;
+          }
+          if (!rv) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) e[j] = 0.f;
+          }
+          stage_bf16_window(buf, row_in_tile, c, e);
+          if (c & 1) {
+            fence_proxy_async_smem();
+            named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
+            if (out_leader) {
+              tma_store_2d(&tmD, n * BN + (c >> 1) * G_SLICE_COLS, P.out_row0 + row0, buf);
               bulk_commit();
             }
             ++slice;
@@ -385,7 +517,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           fence_proxy_async_smem();
           named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
           if (out_leader) {
-            const int y = P.out_row0 + s * P.split_rows + m * BM;
+            const int y = P.out_row0 + s * P.split_rows + row0;
             if (P.reduce_add) tma_reduce_add_2d(&tmD, col0, y, buf);
             else tma_store_2d(&tmD, col0, y, buf);
             bulk_commit();
@@ -393,11 +525,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           ++slice;
         }
       }
-      // release the accumulator buffer to the MMA warp
+      // release the accumulator buffer to the MMA warp (the leader's, for a pair)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
-      if constexpr (EPI == EPI_FWD) {
+      if (lane == 0) {
+        if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(tempty0 + 8u * acc, 0));
+        else mbar_arrive(tempty0 + 8u * acc);
+      }
+      if constexpr (EPI == EPI_FWD || EPI == EPI_FWD_E) {
         if (rv) {
           const size_t o = static_cast<size_t>(n) * P.ld_part + r;
           P.part_m[o] = run_m;
@@ -412,10 +547,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (threadIdx.x == 2 * 32) bulk_wait0();  // output stores complete before the CTA exits
   }
   __syncthreads();
+  // a pair stays resident until neither CTA touches the other's memory any more
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
   }
 }
 

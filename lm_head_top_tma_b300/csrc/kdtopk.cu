@@ -12,6 +12,9 @@
 //   backward  logits GEMM again with G = M softmax - p formed in the epilogue
 //             (bf16 [chunk, V] operand), dH = G W (split-K, then a reduction),
 //             dW += G^T H (fp32 read-modify-write of the caller's dW)
+// The no-recompute fused step keeps the forward's tile-normalised exponentials
+// in the G buffer and forms G from them elementwise once lse is known, so the
+// backward starts at dH.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -23,6 +26,7 @@
 #include <vector>
 
 #include "kd_aux.cuh"
+#include "kd_cache.cuh"
 #include "kd_gemm.cuh"
 #include "kdtopk.h"
 
@@ -114,6 +118,16 @@ int dw_group_rows() {
   return v;
 }
 
+// CTA-pair (two-CTA cluster, 256-row tile) GEMMs for chunks of at least 256
+// rows when KD_PAIR=1 (read once per process); otherwise the single-CTA form.
+bool pair_enabled() {
+  static bool v = [] {
+    const char* e = std::getenv("KD_PAIR");
+    return e && std::atoi(e) != 0;
+  }();
+  return v;
+}
+
 uint64_t wait_limit_ns() {
   static uint64_t v = [] {
     const char* e = std::getenv("KD_WAIT_LIMIT_MS");
@@ -153,6 +167,8 @@ void prof_end(int slot, cudaStream_t st) {
 struct Plan {
   int64_t T;
   int d, V, K, C, Cpad, Kpad, nt, S, kbps_dh, nchunks;
+  bool pair;     // chunk GEMMs run as CTA pairs (tiles of 256 rows)
+  int tile_m;    // rows per GEMM tile: 256 for pairs, 128 otherwise
   int dw_group;  // chunks whose G rows one dW GEMM consumes (K = dw_group * C)
   int64_t ldg;
   size_t off_status, off_sidx, off_sp, off_M, off_E, off_pm, off_ps, off_pz, off_Lrow, off_G, off_dhp, total;
@@ -187,7 +203,9 @@ kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* p
   p.V = V;
   p.K = K;
   p.C = static_cast<int>(std::min<int64_t>(chunk, T));
-  p.Cpad = static_cast<int>(align_up(p.C, BM));
+  p.pair = pair_enabled() && align_up(p.C, BM) >= 2 * BM;
+  p.tile_m = p.pair ? 2 * BM : BM;
+  p.Cpad = static_cast<int>(align_up(p.C, p.tile_m));
   p.Kpad = 32;
   while (p.Kpad < K) p.Kpad <<= 1;
   p.nt = static_cast<int>(ceil_div(V, BN));
@@ -197,7 +215,8 @@ kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* p
   p.dw_group = (p.C == p.Cpad) ? std::min(4, std::max(1, dw_group_rows() / p.C)) : 1;
   p.dw_group = std::min(p.dw_group, p.nchunks);
   const int64_t kb_v = ceil_div(V, BK);
-  int S = choose_splits(static_cast<int64_t>(p.Cpad / BM) * ceil_div(d, BN), kb_v, current_sm_count());
+  const int sms = current_sm_count();
+  int S = choose_splits(static_cast<int64_t>(p.Cpad / p.tile_m) * ceil_div(d, BN), kb_v, p.pair ? sms / 2 : sms);
   p.kbps_dh = static_cast<int>(ceil_div(kb_v, S));
   p.S = static_cast<int>(ceil_div(kb_v, p.kbps_dh));
   size_t o = 0;
@@ -227,20 +246,58 @@ kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* p
   return KD_OK;
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+// Persistent launch: one CTA (or CTA pair) per SM, at most one per tile.
+template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 cudaError_t launch_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                         const GemmParams& P, int sms, cudaStream_t st) {
-  auto kern = kd_gemm_kernel<EPI, A_MN, B_MN>;
-  constexpr size_t smem = gemm_smem_bytes(EPI);
+  auto kern = kd_gemm_kernel<EPI, A_MN, B_MN, PAIR>;
+  constexpr size_t smem = gemm_smem_bytes<PAIR>(EPI);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int64_t tiles = static_cast<int64_t>(P.num_m) * P.num_n * P.num_s;
-  const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
   const int slot = prof_begin(kind, st);
-  kern<<<grid, GEMM_THREADS, smem, st>>>(ta, tb, td, P);
-  e = cudaGetLastError();
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // pairs that can be resident at once (clusters sit within one GPC), asked once per kernel
+    static int resident = 0;
+    if (resident == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(std::max(2, sms)));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = std::max(1, sms / 2);
+      }
+      resident = n;
+    }
+    const int pairs = static_cast<int>(std::min<int64_t>(tiles, std::min(resident, std::max(1, sms / 2))));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, td, P);
+  } else {
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
+    kern<<<grid, GEMM_THREADS, smem, st>>>(ta, tb, td, P);
+    e = cudaGetLastError();
+  }
   prof_end(slot, st);
   return e;
+}
+
+// Dispatch on the pair form chosen at run time.
+template <int EPI, bool A_MN, bool B_MN>
+cudaError_t launch_gemm_any(bool pair, int kind, const CUtensorMap& ta, const CUtensorMap& tb,
+                            const CUtensorMap& td, const GemmParams& P, int sms, cudaStream_t st) {
+  return pair ? launch_gemm<EPI, A_MN, B_MN, true>(kind, ta, tb, td, P, sms, st)
+              : launch_gemm<EPI, A_MN, B_MN, false>(kind, ta, tb, td, P, sms, st);
 }
 
 GemmParams base_params(int* status) {
@@ -254,7 +311,10 @@ GemmParams base_params(int* status) {
   return P;
 }
 
-enum { MODE_FWD = 1, MODE_BWD = 2 };
+// MODE_KEEP (with MODE_FWD | MODE_BWD): the forward GEMM keeps the chunk's
+// tile-normalised exponentials in the G buffer and an elementwise pass turns
+// them into G, instead of recomputing the logits in the backward.
+enum { MODE_FWD = 1, MODE_BWD = 2, MODE_KEEP = 4 };
 
 kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const float* p, const float* lse_in,
               int64_t T, int d, int V, int K, int chunk, float dloss, float* loss, float* lse, float* loss_rows,
@@ -293,7 +353,9 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   // TMA descriptors (all bf16, 128-byte swizzle, 64-element inner boxes)
   CUtensorMap tmH_k, tmW_k, tmG_k, tmW_mn, tmG_mn, tmH_mn, tmDhp, tmDW;
   const uint64_t hrow = uint64_t(d) * 2;
-  bool ok = tmap_bf16(&tmH_k, H, d, T, hrow, BK, BM) && tmap_bf16(&tmW_k, W, d, V, hrow, BK, BN);
+  const bool pr = pl.pair;
+  // K-major B (W in the logits GEMMs): each CTA of a pair stages half of the 256 columns
+  bool ok = tmap_bf16(&tmH_k, H, d, T, hrow, BK, BM) && tmap_bf16(&tmW_k, W, d, V, hrow, BK, pr ? BN / 2 : BN);
   if (mode & MODE_BWD) {
     const uint64_t grows = uint64_t(pl.dw_group) * pl.Cpad;  // G rows held in the workspace
     ok = ok && tmap_bf16(&tmG_k, G, V, grows, uint64_t(pl.ldg) * 2, BK, BM) &&
@@ -313,9 +375,12 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
                            static_cast<int>(prep_smem)) != cudaSuccess)
     return KD_ERR_CUDA;
 
+  const bool keep = (mode & MODE_KEEP) != 0;
   for (int c = 0; c < pl.nchunks; ++c) {
     const int64_t t0 = int64_t(c) * pl.C;
     const int rows = static_cast<int>(std::min<int64_t>(pl.C, T - t0));
+    const int gslot = c % pl.dw_group;  // this chunk's G rows: [gslot * Cpad, +Cpad)
+    __nv_bfloat16* Gc = G + size_t(gslot) * pl.Cpad * pl.ldg;
     cudaError_t e;
     // -------- prep
     {
@@ -327,7 +392,7 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       if (e != cudaSuccess) return KD_ERR_CUDA;
     }
     GemmParams L = base_params(status);
-    L.num_m = pl.Cpad / BM;
+    L.num_m = pl.Cpad / pl.tile_m;
     L.num_n = pl.nt;
     L.kb_total = L.kb_per_split = static_cast<int>(ceil_div(d, BK));
     L.a_mn0 = static_cast<int>(t0);
@@ -343,8 +408,15 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       P.part_s = ps;
       P.part_pz = ppz;
       P.ld_part = pl.Cpad;
-      if (launch_gemm<EPI_FWD, false, false>(KD_K_LOGITS_FWD, tmH_k, tmW_k, tmH_k, P, sms, st) != cudaSuccess)
+      if (keep) {
+        P.out_row0 = gslot * pl.Cpad;
+        if (launch_gemm_any<EPI_FWD_E, false, false>(pr, KD_K_LOGITS_FWD, tmH_k, tmW_k, tmG_k, P, sms, st) !=
+            cudaSuccess)
+          return KD_ERR_CUDA;
+      } else if (launch_gemm_any<EPI_FWD, false, false>(pr, KD_K_LOGITS_FWD, tmH_k, tmW_k, tmH_k, P, sms, st) !=
+                 cudaSuccess) {
         return KD_ERR_CUDA;
+      }
       const int slot = prof_begin(KD_K_COMBINE, st);
       kd_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, 32)), COMBINE_WARPS * 32, 0, st>>>(
           pm, ps, ppz, pl.nt, pl.Cpad, rows, rowM, rowE, lse + t0, loss_rows ? loss_rows + t0 : nullptr, Lrow);
@@ -353,26 +425,36 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       e = cudaGetLastError();
       prof_end(slot, st);
       if (e != cudaSuccess) return KD_ERR_CUDA;
+      if (keep) {  // G from the kept exponentials, in place, now that lse is known
+        const int gs = prof_begin(KD_K_G_FROM_E, st);
+        kd_g_from_e_kernel<<<static_cast<unsigned>(rows), GPASS_THREADS, 0, st>>>(Gc, pl.ldg, rows, V, K, sidx, sp,
+                                                                               rowM, lse + t0, pm, pl.Cpad);
+        e = cudaGetLastError();
+        prof_end(gs, st);
+        if (e != cudaSuccess) return KD_ERR_CUDA;
+      }
     }
     // -------- backward: G, dH, dW
     if (mode & MODE_BWD) {
-      const int gslot = c % pl.dw_group;  // this chunk's G rows: [gslot * Cpad, +Cpad)
-      GemmParams P = L;
-      P.out_row0 = gslot * pl.Cpad;
-      P.rowM = rowM;
-      P.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0;
-      if (launch_gemm<EPI_G, false, false>(KD_K_LOGITS_G, tmH_k, tmW_k, tmG_k, P, sms, st) != cudaSuccess)
-        return KD_ERR_CUDA;
+      if (!keep) {
+        GemmParams P = L;
+        P.out_row0 = gslot * pl.Cpad;
+        P.rowM = rowM;
+        P.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0;
+        if (launch_gemm_any<EPI_G, false, false>(pr, KD_K_LOGITS_G, tmH_k, tmW_k, tmG_k, P, sms, st) !=
+            cudaSuccess)
+          return KD_ERR_CUDA;
+      }
 
       GemmParams Q = base_params(status);  // dH partials = G W, split over V
-      Q.num_m = pl.Cpad / BM;
+      Q.num_m = pl.Cpad / pl.tile_m;
       Q.num_n = static_cast<int>(ceil_div(d, BN));
       Q.num_s = pl.S;
       Q.kb_total = static_cast<int>(ceil_div(V, BK));
       Q.kb_per_split = pl.kbps_dh;
       Q.split_rows = pl.Cpad;
       Q.a_mn0 = gslot * pl.Cpad;
-      if (launch_gemm<EPI_F32, false, true>(KD_K_GEMM_DH, tmG_k, tmW_mn, tmDhp, Q, sms, st) != cudaSuccess)
+      if (launch_gemm_any<EPI_F32, false, true>(pr, KD_K_GEMM_DH, tmG_k, tmW_mn, tmDhp, Q, sms, st) != cudaSuccess)
         return KD_ERR_CUDA;
       {
         const int64_t n4 = int64_t(rows) * d / 4;
@@ -388,14 +470,14 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
         // dW (+)= G^T H over the group's chunks, fp32; the first group stores, the rest add in L2
         const int first = c - gslot;
         GemmParams R = base_params(status);
-        R.num_m = static_cast<int>(ceil_div(V, BM));
+        R.num_m = static_cast<int>(ceil_div(V, pl.tile_m));
         R.num_n = static_cast<int>(ceil_div(d, BN));
         R.m_fast = 0;
         R.kb_total = R.kb_per_split = (gslot + 1) * pl.Cpad / BK;
         R.b_k0 = static_cast<int>(int64_t(first) * pl.C);
         R.reduce_add = (first == 0 && !accumulate) ? 0 : 1;
         R.scale = dloss;
-        if (launch_gemm<EPI_F32, true, true>(KD_K_GEMM_DW, tmG_mn, tmH_mn, tmDW, R, sms, st) != cudaSuccess)
+        if (launch_gemm_any<EPI_F32, true, true>(pr, KD_K_GEMM_DW, tmG_mn, tmH_mn, tmDW, R, sms, st) != cudaSuccess)
           return KD_ERR_CUDA;
       }
     }
@@ -436,6 +518,37 @@ kd_status kd_topk_kl_fused_step(const void* H, const void* W, const int32_t* idx
              accumulate_dW, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
+kd_status kd_topk_kl_fused_step_norecompute(const void* H, const void* W, const int32_t* idx, const float* p,
+                                            int64_t T, int d, int V, int K, int chunk, float dloss, float* loss,
+                                            float* lse, float* loss_rows, float* dH, float* dW, int accumulate_dW,
+                                            void* workspace, size_t ws_bytes, void* stream) {
+  return run(MODE_FWD | MODE_BWD | MODE_KEEP, H, W, idx, p, nullptr, T, d, V, K, chunk, dloss, loss, lse,
+             loss_rows, dH, dW, accumulate_dW, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, int V, int K, int32_t* idx,
+                              float* p, float* lse, void* stream) {
+  if (!logits || !idx || !p || T < 1 || V < 1 || K < 1 || K > V) return KD_ERR_INVALID_ARG;
+  if (K > 1024) return KD_ERR_UNSUPPORTED;
+  const uintptr_t need = logits_bf16 ? 1u : 3u;
+  if ((reinterpret_cast<uintptr_t>(logits) & need) || (reinterpret_cast<uintptr_t>(idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(p) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return KD_ERR_UNSUPPORTED;
+  if (!device_supported()) return KD_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int blocks = static_cast<int>(std::min<int64_t>(T, 2LL * current_sm_count()));
+  const int slot = prof_begin(KD_K_OTHER, st);
+  if (logits_bf16)
+    kd_topk_cache_kernel<__nv_bfloat16><<<blocks, CACHE_THREADS, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(logits), T, V, K, idx, p, lse);
+  else
+    kd_topk_cache_kernel<float><<<blocks, CACHE_THREADS, 0, st>>>(static_cast<const float*>(logits), T, V, K, idx,
+                                                                    p, lse);
+  const cudaError_t e = cudaGetLastError();
+  prof_end(slot, st);
+  return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
 kd_status kd_topk_kl_device_status(void* workspace, void* stream) {
   if (!workspace) return KD_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -461,7 +574,7 @@ const char* kd_status_string(kd_status s) {
 }
 
 kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int K, int lda, int ldb, int ldd,
-                       int a_mn, int b_mn, void* workspace, size_t ws_bytes, void* stream) {
+                       int a_mn, int b_mn, int cta_pair, void* workspace, size_t ws_bytes, void* stream) {
   if (!A || !B || !D || !workspace || M < 1 || N < 1 || K < 1) return KD_ERR_INVALID_ARG;
   if (ws_bytes < 256) return KD_ERR_WORKSPACE;
   if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (lda % 8) || (ldb % 8) || (ldd % 4))
@@ -472,25 +585,27 @@ kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int
   int* status = static_cast<int*>(workspace);
   CUtensorMap ta, tb;
   bool ok = a_mn ? tmap_bf16(&ta, A, M, K, uint64_t(lda) * 2, 64, BK) : tmap_bf16(&ta, A, K, M, uint64_t(lda) * 2, BK, BM);
-  ok = ok && (b_mn ? tmap_bf16(&tb, B, N, K, uint64_t(ldb) * 2, 64, BK) : tmap_bf16(&tb, B, K, N, uint64_t(ldb) * 2, BK, BN));
+  const bool pr = cta_pair != 0;
+  ok = ok && (b_mn ? tmap_bf16(&tb, B, N, K, uint64_t(ldb) * 2, 64, BK)
+                   : tmap_bf16(&tb, B, K, N, uint64_t(ldb) * 2, BK, pr ? BN / 2 : BN));
   CUtensorMap td;
   ok = ok && tmap_f32_out(&td, D, N, M, uint64_t(ldd) * 4);
   if (!ok) return KD_ERR_CUDA;
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
   GemmParams P = base_params(status);
-  P.num_m = static_cast<int>(ceil_div(M, BM));
+  P.num_m = static_cast<int>(ceil_div(M, pr ? 2 * BM : BM));
   P.num_n = static_cast<int>(ceil_div(N, BN));
   P.kb_total = P.kb_per_split = static_cast<int>(ceil_div(K, BK));
   const int sms = current_sm_count();
   cudaError_t e;
-  if (!a_mn && !b_mn) e = launch_gemm<EPI_F32, false, false>(KD_K_OTHER, ta, tb, td, P, sms, st);
-  else if (!a_mn && b_mn) e = launch_gemm<EPI_F32, false, true>(KD_K_OTHER, ta, tb, td, P, sms, st);
-  else if (a_mn && !b_mn) e = launch_gemm<EPI_F32, true, false>(KD_K_OTHER, ta, tb, td, P, sms, st);
-  else e = launch_gemm<EPI_F32, true, true>(KD_K_OTHER, ta, tb, td, P, sms, st);
+  if (!a_mn && !b_mn) e = launch_gemm_any<EPI_F32, false, false>(pr, KD_K_OTHER, ta, tb, td, P, sms, st);
+  else if (!a_mn && b_mn) e = launch_gemm_any<EPI_F32, false, true>(pr, KD_K_OTHER, ta, tb, td, P, sms, st);
+  else if (a_mn && !b_mn) e = launch_gemm_any<EPI_F32, true, false>(pr, KD_K_OTHER, ta, tb, td, P, sms, st);
+  else e = launch_gemm_any<EPI_F32, true, true>(pr, KD_K_OTHER, ta, tb, td, P, sms, st);
   return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
-kd_status kd_debug_wait_timeout(int wait_limit_ms, void* workspace, size_t ws_bytes, void* stream) {
+kd_status kd_debug_wait_timeout(int wait_limit_ms, int cta_pair, void* workspace, size_t ws_bytes, void* stream) {
   if (!workspace || wait_limit_ms < 1 || wait_limit_ms > 10000) return KD_ERR_INVALID_ARG;
   if (ws_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KD_ERR_WORKSPACE;
   if (!device_supported()) return KD_ERR_UNSUPPORTED;
@@ -508,7 +623,10 @@ kd_status kd_debug_wait_timeout(int wait_limit_ms, void* workspace, size_t ws_by
   P.num_m = 1;
   P.num_n = 1;
   P.kb_total = P.kb_per_split = 2;
-  if (launch_gemm<EPI_F32, false, false>(KD_K_OTHER, ta, tb, td, P, 1, st) != cudaSuccess) return KD_ERR_CUDA;
+  // one CTA, or one pair of CTAs
+  if (launch_gemm_any<EPI_F32, false, false>(cta_pair != 0, KD_K_OTHER, ta, tb, td, P, cta_pair ? 2 : 1, st) !=
+      cudaSuccess)
+    return KD_ERR_CUDA;
   return kd_topk_kl_device_status(workspace, stream);
 }
 
@@ -546,8 +664,8 @@ int kd_profile_read(double* ms_total, int64_t* launches, int n, int reset) {
 }
 
 const char* kd_profile_kind_name(int kind) {
-  static const char* names[KD_PROF_KINDS] = {"prep",        "logits_fwd", "combine",   "logits_g",
-                                             "gemm_dh",     "dh_reduce",  "gemm_dw",   "other"};
+  static const char* names[KD_PROF_KINDS] = {"prep",    "logits_fwd", "combine", "logits_g", "gemm_dh",
+                                             "dh_reduce", "gemm_dw",   "other",   "g_from_e"};
   return (kind >= 0 && kind < KD_PROF_KINDS) ? names[kind] : "unknown";
 }
 

@@ -40,7 +40,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "sweep_workload", "get_workload",
-           "make_cache", "make_hw", "make_inputs"]
+           "make_cache", "make_hw", "make_inputs", "make_teacher_logits"]
 
 
 @dataclass(frozen=True)
@@ -198,3 +198,31 @@ def make_inputs(workload, device="cpu", T: int | None = None, seed: int | None =
     H, W = make_hw(wl.T, wl.d, wl.V, wl.kind, wl.seed, device=device)
     idx, p = make_cache(wl.T, wl.V, wl.K, wl.kind, wl.seed)
     return {"H": H, "W": W, "idx": idx, "p": p, "workload": wl}
+
+
+# ----------------------------------------------------------------------------
+# teacher logits (input of the cache builder)
+# ----------------------------------------------------------------------------
+
+def make_teacher_logits(T: int, V: int, seed: int, device="cpu", dtype="bf16",
+                        zipf_s: float = 1.1, noise: float = 2.0, block: int = 4096):
+    """Synthetic teacher logits Z [T,V] on ``device``: a Zipf-shaped prior over
+    a seeded vocabulary ranking plus per-token Gaussian noise,
+    z_tj = -s log(1 + rank(j)) + noise * N(0, 1), rounded to ``dtype``
+    ("bf16" or "fp32").  The top-K ids of such rows follow the same
+    rank-permuted Zipf law as ``make_cache``'s ids; bf16 rounding leaves many
+    exactly equal logits, so the builder's tie order is exercised."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    perm = torch.randperm(V, generator=g, device=device)
+    prior = torch.empty(V, dtype=torch.float32, device=device)
+    prior[perm] = -zipf_s * torch.log1p(torch.arange(V, dtype=torch.float32, device=device))
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    out = torch.empty(T, V, dtype=tdt, device=device)
+    for r0 in range(0, T, block):
+        n = min(block, T - r0)
+        x = torch.randn(n, V, generator=g, device=device, dtype=torch.float32)
+        out[r0:r0 + n] = (prior[None, :] + noise * x).to(tdt)
+    return out

@@ -68,9 +68,10 @@ def fused_to_host(res: dict) -> dict:
     return out
 
 
-def run_fused(H, W, idx_np, p_np, chunk, **kw):
+def run_fused(H, W, idx_np, p_np, chunk, recompute=True, **kw):
     idx, p = to_dev(idx_np, p_np, H.device)
-    return fused_to_host(api.fused_step(H, W, idx, p, chunk, loss_rows=True, **kw))
+    fn = api.fused_step if recompute else api.fused_step_norecompute
+    return fused_to_host(fn(H, W, idx, p, chunk, loss_rows=True, **kw))
 
 
 __all__ = ["kd_oracle", "kd_oracle_rows", "to_dev", "grad_err", "assert_close_full", "fused_to_host",

@@ -12,10 +12,11 @@ from lm_head_top_tma_b300 import api
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_timeout_is_reported_and_context_survives(cuda_device):
-    assert api.debug_wait_timeout(50, cuda_device) == N.KD_ERR_TIMEOUT
-    A = torch.ones(128, 64, device=cuda_device, dtype=torch.bfloat16)
-    D = api.gemm_bf16(A, A, 128, 128, 64)
+@pytest.mark.parametrize("pair", [False, True])
+def test_wait_timeout_is_reported_and_context_survives(cuda_device, pair):
+    assert api.debug_wait_timeout(50, cuda_device, cta_pair=pair) == N.KD_ERR_TIMEOUT
+    A = torch.ones(256, 64, device=cuda_device, dtype=torch.bfloat16)
+    D = api.gemm_bf16(A, A, 256, 256, 64, cta_pair=pair)
     torch.cuda.synchronize()
     assert torch.all(D == 64.0)
 
