@@ -89,6 +89,10 @@ typedef enum kd_status {
  * consecutive chunks (up to 4096 rows, at most 4 chunks; environment variable
  * KD_DW_GROUP_ROWS, read once per process, changes the row target, 0 turns it
  * off) and runs one dW GEMM per group; the workspace size includes it.
+ * Chunks of 256 rows or more run their GEMMs on two-CTA clusters (256-row
+ * tiles; the chunk's rows are padded to a multiple of 256 in the workspace);
+ * environment variable KD_PAIR=0 (read once per process) selects one CTA per
+ * 128-row tile instead.
  */
 KD_API size_t kd_topk_kl_workspace_size(int64_t T, int d, int V, int K, int chunk, int what);
 

@@ -119,11 +119,11 @@ int dw_group_rows() {
 }
 
 // CTA-pair (two-CTA cluster, 256-row tile) GEMMs for chunks of at least 256
-// rows when KD_PAIR=1 (read once per process); otherwise the single-CTA form.
+// rows; KD_PAIR=0 (read once per process) selects the single-CTA form.
 bool pair_enabled() {
   static bool v = [] {
     const char* e = std::getenv("KD_PAIR");
-    return e && std::atoi(e) != 0;
+    return !(e && std::atoi(e) == 0);
   }();
   return v;
 }
