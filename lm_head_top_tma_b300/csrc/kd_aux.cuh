@@ -93,9 +93,10 @@ __global__ void __launch_bounds__(PREP_WARPS * 32)
   }
 }
 
-constexpr int COMBINE_WARPS = 8;
+constexpr int COMBINE_WARPS = 32;
 
-// Block = 32 rows x 8 warps; warp w folds vocabulary tiles w, w+8, ...
+// Block = 32 rows x 32 warps; warp w folds vocabulary tiles w, w+32, ...
+// (four loads in flight per thread), warp 0 folds the 32 warp results.
 __global__ void __launch_bounds__(COMBINE_WARPS * 32)
     kd_combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
                       const float* __restrict__ ppz, int nt, int ld_part, int rows_valid,
@@ -107,15 +108,26 @@ __global__ void __launch_bounds__(COMBINE_WARPS * 32)
   const int r = blockIdx.x * 32 + lane;
   float m = -INFINITY, s = 0.f, z = 0.f;
   if (r < rows_valid) {
-    for (int t = warp; t < nt; t += COMBINE_WARPS) {
-      const size_t o = static_cast<size_t>(t) * ld_part + r;
-      const float a = pm[o], b = ps[o];
-      z += ppz[o];
-      if (a > m) {
-        s = s * ex2(m - a) + b;
-        m = a;
-      } else if (a > -INFINITY) {
-        s += b * ex2(a - m);
+    constexpr int U = 4;
+    for (int t0 = warp; t0 < nt; t0 += COMBINE_WARPS * U) {
+      float a[U], b[U], c[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int t = t0 + u * COMBINE_WARPS;
+        const size_t o = static_cast<size_t>(t) * ld_part + r;
+        a[u] = t < nt ? pm[o] : -INFINITY;
+        b[u] = t < nt ? ps[o] : 0.f;
+        c[u] = t < nt ? ppz[o] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        z += c[u];
+        if (a[u] > m) {
+          s = s * ex2(m - a[u]) + b[u];
+          m = a[u];
+        } else if (a[u] > -INFINITY) {
+          s += b[u] * ex2(a[u] - m);
+        }
       }
     }
   }

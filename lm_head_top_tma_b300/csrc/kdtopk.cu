@@ -536,15 +536,29 @@ kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, in
     return KD_ERR_UNSUPPORTED;
   if (!device_supported()) return KD_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int blocks = static_cast<int>(std::min<int64_t>(T, 2LL * current_sm_count()));
+  // 16-byte loads when every row starts on a 16-byte boundary
+  const bool vec = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (int64_t(V) * (logits_bf16 ? 2 : 4)) % 16 == 0;
   const int slot = prof_begin(KD_K_OTHER, st);
-  if (logits_bf16)
-    kd_topk_cache_kernel<__nv_bfloat16><<<blocks, CACHE_THREADS, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(logits), T, V, K, idx, p, lse);
-  else
-    kd_topk_cache_kernel<float><<<blocks, CACHE_THREADS, 0, st>>>(static_cast<const float*>(logits), T, V, K, idx,
-                                                                    p, lse);
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  auto launch = [&](auto kern, const auto* z) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CACHE_THREADS, 0) != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    const int blocks = static_cast<int>(std::min<int64_t>(T, int64_t(per_sm) * current_sm_count()));
+    kern<<<blocks, CACHE_THREADS, 0, st>>>(z, T, V, K, idx, p, lse);
+    e = cudaGetLastError();
+  };
+  if (logits_bf16) {
+    const auto* z = static_cast<const __nv_bfloat16*>(logits);
+    if (vec) launch(kd_topk_cache_kernel<__nv_bfloat16, true>, z);
+    else launch(kd_topk_cache_kernel<__nv_bfloat16, false>, z);
+  } else {
+    const auto* z = static_cast<const float*>(logits);
+    if (vec) launch(kd_topk_cache_kernel<float, true>, z);
+    else launch(kd_topk_cache_kernel<float, false>, z);
+  }
   prof_end(slot, st);
   return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }

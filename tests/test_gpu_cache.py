@@ -69,6 +69,20 @@ def test_ties_and_fallback(cuda_device):
     assert idx[2].tolist() == list(range(5000, 5000 + K))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_signed_zeros_tie(cuda_device, dtype):
+    """-0.0 and +0.0 are equal logits: they tie and go by ascending id."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    Z = torch.full((2, 4096), -3.0, device=cuda_device, dtype=tdt)
+    Z[0, 10::400] = -0.0
+    Z[0, 11::400] = 0.0
+    Z[1, 4000:] = 0.0
+    Z[1, :50] = -0.0
+    idx, _ = check(Z, 40)
+    assert idx[0, :4].tolist() == [10, 11, 410, 411]
+    assert idx[1, :3].tolist() == [0, 1, 2]
+
+
 def test_fp32_fallback_and_negative_values(cuda_device):
     Z = torch.full((3, 9000), -2.25, device=cuda_device)
     Z[1, 100:4200] = 3.0          # 4100 equal maxima

@@ -53,6 +53,11 @@ def test_tiny_forward_then_backward(tiny):
     (300, 256, 4096, 1, 128),      # K = 1 (cross-entropy)
     (64, 128, 512, 512, 64),       # K = V (full distribution)
     (200, 96, 2056, 100, 77),      # odd chunk
+    # chunks of >= 256 rows run on two-CTA clusters (256-row tiles):
+    (600, 200, 4000, 16, 256),     # ragged T, d tail in every GEMM, V % 256 != 0
+    (513, 64, 300, 9, 513),        # 3 pair tiles, one ragged row; the peer's half of the
+                                   # second vocabulary tile lies wholly past V
+    (1100, 136, 1030, 32, 1024),   # two chunks of a pair-tiled size, dW grouped over both
 ])
 def test_edge_shapes(cuda_device, T, d, V, K, chunk):
     H, W = make_hw(T, d, V, "uniform", seed=T + V, device=cuda_device)
