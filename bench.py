@@ -23,7 +23,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -36,13 +35,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); peak bytes vs T"
 
-# DRAM traffic of the dominant kernel from an ncu capture (see profiles/);
-# reported only while the kernel sources still hash to what was captured.
-# dW GEMM, one 2048-row chunk of the long-context head: the first chunk stores dW
-# (2.060 GB), every later chunk reduce-adds into it (3.631 GB); bench lines
-# weight the two by the launch mix (profiles/gemm_traffic_longctx_chunk2048.md).
-TRAFFIC = {"kernel": "gemm_dw", "workload": "longctx", "store_bytes": 538509824 + 1521478912,
-           "accumulate_bytes": 2115711744 + 1515372288, "src_sha": "36c65d452f0810f7"}
+# DRAM traffic of the dominant kernel from an ncu capture (profiles/gemm_traffic_longctx_chunk2048.md);
+# reported only while the kernel sources still hash to what was captured.  dW GEMM (pair form), one
+# launch per group of two 2048-row chunks of the long-context head: the first group stores dW
+# (3.120 GB), every later group reduce-adds into it (4.289 GB); bench lines weight the two by the
+# launch mix.
+TRAFFIC = {"kernel": "gemm_dw", "workload": "longctx", "store_bytes": 1574785792 + 1544741120,
+           "accumulate_bytes": 2751875840 + 1536651264, "src_sha": "536786b56684b548"}
 KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300/csrc/kd_ptx.cuh",
                   "lm_head_top_tma_b300/csrc/kdtopk.cu"]
 
@@ -354,7 +353,6 @@ def run_kdtopk(args):
             "launches_per_step": {k: v[1] // args.steps for k, v in prof_nr.items() if v[1]},
             "clocks": clk_nr}
 
-    nchunks = math.ceil(T / C)
     flops_8 = 8.0 * T * V * d
     flops_6 = 6.0 * T * V * d
     peaks = load_peaks()
@@ -368,8 +366,9 @@ def run_kdtopk(args):
     achieved = per_launch_flops / (dom_ms / dom_n / 1e3) / 1e12 if per_launch_flops and dom_n else None
     traffic = None
     if (TRAFFIC["kernel"] == dom and TRAFFIC["workload"] == wl.name and C == get_workload(wl.name).chunk
-            and TRAFFIC["src_sha"] == kernel_src_sha()):
-        traffic = (TRAFFIC["store_bytes"] + (nchunks - 1) * TRAFFIC["accumulate_bytes"]) / nchunks
+            and TRAFFIC["src_sha"] == kernel_src_sha() and dom_n):
+        n_launch = dom_n // args.steps  # the first launch of a step stores dW, the rest accumulate
+        traffic = (TRAFFIC["store_bytes"] + (n_launch - 1) * TRAFFIC["accumulate_bytes"]) / n_launch
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sustained"],
                 "unit": "TFLOP/s", "frac": (achieved / peaks["bf16_sustained"]) if achieved else None,
                 "traffic": traffic, "peak_kind": f"bf16 sustained ({peaks['source']})",
@@ -474,7 +473,7 @@ def run_topk_cache(args):
     T, V, K = args.T or 32768, 128256, 100
     Z = make_teacher_logits(T, V, seed=7, device=dev, dtype="bf16")
     for _ in range(max(3, args.warmup)):
-        api.topk_cache_build(Z, K)
+        api.topk_cache_build(Z, K, check=False)
     torch.cuda.synchronize(dev)
     api.profile_enable(True)
     api.profile_read(reset=True)
@@ -485,7 +484,7 @@ def run_topk_cache(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        api.topk_cache_build(Z, K)
+        api.topk_cache_build(Z, K, check=False)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()

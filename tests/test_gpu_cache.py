@@ -49,7 +49,9 @@ def test_teacher_like_rows(cuda_device, dtype, V, K):
 
 
 @pytest.mark.parametrize("T,V,K", [(5, 300, 5), (3, 64, 64), (7, 1000, 1), (4, 5000, 1024), (2, 1024, 1024),
-                                   (1, 1, 1), (9, 2047, 33)])
+                                   (1, 1, 1), (9, 2047, 33),
+                                   (3000, 520, 7),       # many short rows per block through the copy ring
+                                   (700, 16392, 100)])   # rows of two chunks, the second nearly empty
 def test_shapes(cuda_device, T, V, K):
     Z = make_teacher_logits(T, V, seed=T * V + K, device=cuda_device, dtype="bf16")
     check(Z, K)
