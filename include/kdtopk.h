@@ -193,16 +193,13 @@ KD_API kd_status kd_topk_kl_forward_noalloc(const void* H, const void* W, const 
  *   lse[t]        log sum_j exp(z_tj) (fp32, device, [T]; may be NULL).
  * Temperature 1; -0 and +0 are equal logits; -inf logits carry no
  * probability.  1 <= K <= min(V, 1024) (KD_ERR_INVALID_ARG /
- * KD_ERR_UNSUPPORTED otherwise).  `workspace` (device, >= 256 bytes, 256-byte
- * aligned) holds the status word: a timed-out internal wait is reported as
- * KD_ERR_TIMEOUT by kd_topk_kl_device_status(workspace).  Rows whose length in
- * bytes is a multiple of 16 (with a 16-byte aligned base) stream through
- * shared memory by bulk copies; others use plain loads.  Allocates nothing;
- * asynchronous on `stream`.
+ * KD_ERR_UNSUPPORTED otherwise).  Rows whose length in bytes is a multiple
+ * of 16 (with a 16-byte aligned base) are read with 16-byte loads, others
+ * element by element.  Allocates nothing, waits on nothing (no device-side
+ * errors are possible); asynchronous on `stream`.
  */
 KD_API kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, int V, int K,
-                                     int32_t* idx, float* p, float* lse, void* workspace, size_t ws_bytes,
-                                     void* stream);
+                                     int32_t* idx, float* p, float* lse, void* stream);
 
 /*
  * Waits for `stream`, then returns and clears the device-side status the

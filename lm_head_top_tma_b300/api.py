@@ -186,11 +186,10 @@ def _fused(fn, name, H, W, idx, p, chunk, dloss, dW, accumulate_dW, loss_rows, w
     return res
 
 
-def topk_cache_build(Z, K: int, *, lse: bool = True, check: bool = True):
+def topk_cache_build(Z, K: int, *, lse: bool = True):
     """Teacher cache from logits Z [T,V] (bf16 or fp32, CUDA): ids of the K
     largest logits (largest first, ties by ascending id), their softmax
-    probabilities, and lse.  Returns (idx int32 [T,K], p fp32 [T,K], lse fp32 [T] or None).
-    ``check`` waits for the stream and raises on a device-side error."""
+    probabilities, and lse.  Returns (idx int32 [T,K], p fp32 [T,K], lse fp32 [T] or None)."""
     if not isinstance(Z, torch.Tensor) or not Z.is_cuda or Z.dim() != 2 or not Z.is_contiguous():
         raise ValueError("Z must be a contiguous 2-D CUDA tensor")
     if Z.dtype not in (torch.bfloat16, torch.float32):
@@ -200,11 +199,9 @@ def topk_cache_build(Z, K: int, *, lse: bool = True, check: bool = True):
     idx = torch.empty(T, K, dtype=torch.int32, device=dev)
     p = torch.empty(T, K, dtype=torch.float32, device=dev)
     l = torch.empty(T, dtype=torch.float32, device=dev) if lse else None
-    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
     rc = N.load().kd_topk_cache_build(_ptr(Z), int(Z.dtype == torch.bfloat16), T, V, int(K), _ptr(idx), _ptr(p),
-                                      _ptr(l), _ptr(ws), ws.numel(), _stream(dev))
+                                      _ptr(l), _stream(dev))
     N.check(rc, "kd_topk_cache_build")
-    _finish(ws, dev, "kd_topk_cache_build", check)
     return idx, p, l
 
 

@@ -6,11 +6,9 @@
 // aimodeling.com "First cut": top-100 probabilities cached for every token),
 // here over logits that are already on the device.
 //
-// One block of 512 threads per row (grid-stride over rows, two blocks per SM);
-// the row is read from HBM once and a second time from L2.  Rows whose byte
-// length is a multiple of 16 stream through a ring of bulk copies into shared
-// memory (kd_topk_cache_stream_kernel); other rows use plain loads
-// (kd_topk_cache_kernel).  Both run the same selection:
+// One block of 512 threads per row (grid-stride over rows, several blocks per
+// SM); the row is read from HBM once (16-byte loads, several in flight per
+// thread) and a second time from L2:
 //   pass 1  per-slot maximum key (1024 slots: two per thread, every element in
 //           exactly one) and an online (max, sum of 2^x) for lse;
 //   select  theta = the K-th largest slot maximum, by a binary search over the
@@ -42,10 +40,7 @@ namespace kd {
 constexpr int CACHE_THREADS = 512;
 constexpr int CACHE_SLOTS = 2 * CACHE_THREADS;  // per-row maxima used to bound the K-th key
 constexpr int CACHE_CAP = 4096;                 // candidates kept in shared memory
-constexpr int RING = 4;                         // chunks in flight per block (streaming form)
-constexpr int RING_CHUNK = 16384;               // bytes per chunk, a multiple of 16
-constexpr int RING_GROUPS = RING_CHUNK / 16;    // 16-byte groups per chunk
-static_assert(RING_GROUPS == 2 * CACHE_THREADS, "two groups per thread per chunk");
+constexpr int CACHE_UNROLL = 4;                 // 16-byte loads in flight per thread
 
 template <typename T>
 struct LogitTraits;
@@ -164,330 +159,137 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = mn;
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
-  return r;
-}
+// Element-wise access to one row, as 16-byte vectors when the row allows it;
+// a loaded group stays packed (Raw) until its elements are used.
+template <typename TL, bool VEC>
+struct RowView {
+  const TL* z;
+  int V;
+  static constexpr int PV = VEC ? LogitTraits<TL>::PER_VEC : 1;
+  using Raw = typename std::conditional<VEC, uint4, TL>::type;
+  __device__ int groups() const { return VEC ? V / PV : V; }
+  __device__ Raw load(int g) const {
+    if constexpr (VEC) return __ldg(reinterpret_cast<const uint4*>(z) + g);
+    else return z[g];
+  }
+  __device__ static TL elem(const Raw& r, int i) {
+    if constexpr (VEC) return reinterpret_cast<const TL*>(&r)[i];
+    else return r;
+  }
+  __device__ static void floats(const Raw& r, float (&f)[PV]) {
+    if constexpr (VEC) LogitTraits<TL>::unpack(r, f);
+    else f[0] = LogitTraits<TL>::value(r);
+  }
+};
 
-// theta: the K-th largest of the block's slot keys (two per thread), by a
-// binary search inside the keys' range [lo, hi] with block-wide counts.
-__device__ __forceinline__ uint32_t kth_slot_key(uint32_t k0, uint32_t k1, int K, uint64_t lo, uint64_t hi) {
-  while (lo < hi) {
-    const uint64_t mid = lo + (hi - lo + 1) / 2;
-    const int cnt = __syncthreads_count(k0 >= mid) + __syncthreads_count(k1 >= mid);
-    if (cnt >= K) lo = mid;
-    else hi = mid - 1;
-  }
-  return static_cast<uint32_t>(lo);
-}
-
-// Given the n candidates of one row in cand[] (composite keys (~key << 32) | id,
-// every element with key >= theta; n > CACHE_CAP means only the first
-// CACHE_CAP were kept), orders the row's top K by (key descending, id
-// ascending) and writes idx, p = exp(z - lse).  All threads of the block call it.
-template <typename TL>
-__device__ void select_and_emit(const TL* __restrict__ z, int V, int K, int n, uint32_t theta, uint64_t* cand,
-                                int* red_i, int* s_count, float lse, int32_t* __restrict__ idx_row,
-                                float* __restrict__ p_row) {
-  using Tr = LogitTraits<TL>;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  constexpr int NW = CACHE_THREADS / 32;
-  if (n > CACHE_CAP) {
-    // ---------------- fallback: exact K-th key by binary search, then ordered ties
-    // largest kappa with count(key >= kappa) >= K, searched in [theta, 2^bits - 1]
-    uint64_t lo2 = theta, hi2 = (Tr::KEY_BITS == 32) ? 0xFFFFFFFFull : 0xFFFFull;
-    while (lo2 < hi2) {
-      const uint64_t mid = lo2 + (hi2 - lo2 + 1) / 2;
-      int c = 0;
-      for (int j = tid; j < V; j += CACHE_THREADS) c += static_cast<uint64_t>(Tr::key(z[j])) >= mid;
-      if (block_sum_int(c, red_i) >= K) lo2 = mid;
-      else hi2 = mid - 1;
-    }
-    const uint32_t kappa = static_cast<uint32_t>(lo2);
-    __syncthreads();
-    if (tid == 0) *s_count = 0;
-    __syncthreads();
-    for (int j = tid; j < V; j += CACHE_THREADS) {  // fewer than K are strictly above kappa
-      const uint32_t k = Tr::key(z[j]);
-      if (k > kappa) cand[atomicAdd(s_count, 1)] = (static_cast<uint64_t>(~k) << 32) | static_cast<uint32_t>(j);
-    }
-    __syncthreads();
-    int taken = *s_count;
-    // ties at kappa in ascending id order, one block-wide segment at a time
-    for (int base = 0; base < V && taken < K; base += CACHE_THREADS) {
-      const int j = base + tid;
-      const bool tie = j < V && Tr::key(z[j]) == kappa;
-      const unsigned bal = __ballot_sync(0xffffffffu, tie);
-      __syncthreads();
-      if (lane == 0) red_i[warp] = __popc(bal);
-      __syncthreads();
-      int before = 0;
-      for (int w = 0; w < warp; ++w) before += red_i[w];
-      const int rank_in = before + __popc(bal & ((1u << lane) - 1u));
-      if (tie && taken + rank_in < K)
-        cand[taken + rank_in] = (static_cast<uint64_t>(~kappa) << 32) | static_cast<uint32_t>(j);
-      int total = 0;
-      for (int w = 0; w < NW; ++w) total += red_i[w];
-      taken += total;
-    }
-    n = K;
-    __syncthreads();
-  }
-  if (n <= 2 * CACHE_THREADS) {
-    // rank of each candidate = number of smaller composite keys (all distinct); only owners count
-    uint64_t mine[2];
-    int rank[2] = {0, 0};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) mine[h] = (tid + h * CACHE_THREADS < n) ? cand[tid + h * CACHE_THREADS] : ~0ull;
-    if (tid < n) {
-      if (tid + CACHE_THREADS < n) {
-        for (int j = 0; j < n; ++j) {
-          const uint64_t c = cand[j];
-          rank[0] += c < mine[0];
-          rank[1] += c < mine[1];
-        }
-      } else {
-        for (int j = 0; j < n; ++j) rank[0] += cand[j] < mine[0];
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (tid + h * CACHE_THREADS < n && rank[h] < K) {
-        const int id = static_cast<int>(mine[h] & 0xFFFFFFFFu);
-        idx_row[rank[h]] = id;
-        p_row[rank[h]] = ex2((Tr::value(z[id]) - lse) * kLog2e);
-      }
-    }
-  } else {
-    int n_pad = 1;
-    while (n_pad < n) n_pad <<= 1;
-    for (int i = n + tid; i < n_pad; i += CACHE_THREADS) cand[i] = ~0ull;
-    __syncthreads();
-    block_bitonic_sort_u64(cand, n_pad);
-    for (int k = tid; k < K; k += CACHE_THREADS) {
-      const int id = static_cast<int>(cand[k] & 0xFFFFFFFFu);
-      idx_row[k] = id;
-      p_row[k] = ex2((Tr::value(z[id]) - lse) * kLog2e);
-    }
-  }
-}
-
-// Per-row statistics after pass 1: lse into *s_lse, the slot keys' range into
-// *klo / *khi, and the candidate counter *s_count reset before anyone can add
-// to it (all threads call; valid after the call in every thread).
-__device__ __forceinline__ void row_stats(float m, float s, uint32_t k0, uint32_t k1, float* red_m, float* red_s,
-                                          uint32_t (*red_k)[32], float* s_lse, int* s_count, uint64_t* klo,
-                                          uint64_t* khi) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int NW = CACHE_THREADS / 32;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
-  uint32_t kmin = min(k0, k1), kmax = max(k0, k1);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  __syncthreads();  // the previous row's shared state is no longer read
-  if (lane == 0) {
-    red_m[warp] = m;
-    red_s[warp] = s;
-    red_k[0][warp] = kmin;
-    red_k[1][warp] = kmax;
-  }
-  if (threadIdx.x == 0) *s_count = 0;
-  __syncthreads();
-  if (warp == 0) {
-    float mm = lane < NW ? red_m[lane] : -INFINITY;
-    float ss = lane < NW ? red_s[lane] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      lse_merge(mm, ss, __shfl_xor_sync(0xffffffffu, mm, o), __shfl_xor_sync(0xffffffffu, ss, o));
-    if (lane == 0) *s_lse = mm + log2f(ss) * kLn2;
-  }
-  uint64_t lo = 0xFFFFFFFFull, hi = 0;
-  for (int w = 0; w < NW; ++w) {
-    lo = lo < red_k[0][w] ? lo : red_k[0][w];
-    hi = hi > red_k[1][w] ? hi : red_k[1][w];
-  }
-  *klo = lo;
-  *khi = hi;
-}
-
-// ---------------------------------------------------------------- plain loads (any row length)
-template <typename TL>
+template <typename TL, bool VEC>
 __global__ void __launch_bounds__(CACHE_THREADS, 2)
     kd_topk_cache_kernel(const TL* __restrict__ Z, int64_t T, int V, int K, int32_t* __restrict__ idx_out,
                          float* __restrict__ p_out, float* __restrict__ lse_out) {
   using Tr = LogitTraits<TL>;
+  using RV = RowView<TL, VEC>;
+  constexpr int PV = RV::PV;
   __shared__ uint64_t cand[CACHE_CAP];  // (~key << 32) | id: ascending = key descending, id ascending
   __shared__ float red_m[32], red_s[32];
-  __shared__ uint32_t red_k[2][32];
   __shared__ int red_i[32];
   __shared__ int s_count;
   __shared__ float s_lse;
   const int tid = threadIdx.x;
-  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
-    const TL* z = Z + row * static_cast<int64_t>(V);
-    // pass 1: slot maxima (elements tid, tid + 2*512, ... and tid + 512, ...), normaliser
-    float fslot0 = -INFINITY, fslot1 = -INFINITY, m = -INFINITY, s = 0.f;
-    for (int j = tid; j < V; j += CACHE_THREADS) {
-      const float f[1] = {Tr::value(z[j])};
-      lse_fold(m, s, f[0], f);
-      if ((j / CACHE_THREADS) & 1) fslot1 = fmaxf(fslot1, f[0]);
-      else fslot0 = fmaxf(fslot0, f[0]);
-    }
-    // slots without elements hold -inf: no larger than any element, so they never raise theta
-    const uint32_t k0 = Tr::fkey(fslot0), k1 = Tr::fkey(fslot1);
-    uint64_t lo, hi;
-    row_stats(m, s, k0, k1, red_m, red_s, red_k, &s_lse, &s_count, &lo, &hi);
-    const uint32_t theta = kth_slot_key(k0, k1, K, lo, hi);
-    const float tv = Tr::kvalue(theta);
-    // pass 2: candidates with key >= theta, i.e. value >= theta's value
-    for (int j = tid; j < V; j += CACHE_THREADS) {
-      const float f = Tr::value(z[j]);
-      if (f >= tv) {
-        const int at = atomicAdd(&s_count, 1);
-        if (at < CACHE_CAP) cand[at] = (static_cast<uint64_t>(~Tr::fkey(f)) << 32) | static_cast<uint32_t>(j);
-      }
-    }
-    __syncthreads();
-    select_and_emit<TL>(z, V, K, s_count, theta, cand, red_i, &s_count, s_lse, idx_out + row * K, p_out + row * K);
-    if (tid == 0 && lse_out) lse_out[row] = s_lse;
-  }
-}
-
-// ---------------------------------------------------------------- streaming form
-// Rows whose byte length is a multiple of 16 (16-byte aligned base).  Chunk q
-// of the block's sequence (rows blockIdx.x, + gridDim.x, ...; per row pass 1
-// then pass 2, each ceil(V * size / RING_CHUNK) chunks) is copied into ring
-// slot q % RING by one thread with cp.async.bulk; the slot's "full" barrier
-// counts the bytes, the warps release it on its "empty" barrier, and the copy
-// RING steps ahead is issued as soon as the slot is free, so the next row's
-// loads overlap this row's selection.  Every wait is bounded: on expiry the
-// block records KD_ERR_TIMEOUT, stops waiting and issuing, lets issued copies
-// land (bounded) and its outputs are not to be used.
-template <typename TL>
-__global__ void __launch_bounds__(CACHE_THREADS, 2)
-    kd_topk_cache_stream_kernel(const TL* __restrict__ Z, int64_t T, int V, int K, int32_t* __restrict__ idx_out,
-                                float* __restrict__ p_out, float* __restrict__ lse_out, int* status,
-                                uint64_t wait_ns) {
-  using Tr = LogitTraits<TL>;
-  constexpr int PV = Tr::PER_VEC;
-  extern __shared__ __align__(128) uint8_t ring[];  // RING x RING_CHUNK
-  __shared__ uint64_t cand[CACHE_CAP];
-  __shared__ __align__(8) uint64_t full_bar[RING], empty_bar[RING];
-  __shared__ float red_m[32], red_s[32];
-  __shared__ uint32_t red_k[2][32];
-  __shared__ int red_i[32];
-  __shared__ int s_count;
-  __shared__ volatile int s_abort;
-  __shared__ float s_lse;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
+  const int warp = tid >> 5, lane = tid & 31;
   constexpr int NW = CACHE_THREADS / 32;
 
-  const int64_t row_bytes = static_cast<int64_t>(V) * sizeof(TL);
-  const int nch = static_cast<int>((row_bytes + RING_CHUNK - 1) / RING_CHUNK);
-  const int64_t my_rows = (T - blockIdx.x + gridDim.x - 1) / gridDim.x;
-  const int64_t total = my_rows * 2 * nch;
-  const uint32_t ring0 = smem_u32(ring);
-  const uint32_t full0 = smem_u32(full_bar), empty0 = smem_u32(empty_bar);
-  int64_t issued = 0;  // (thread 0) sequence elements issued so far
-
-  auto issue = [&](int64_t qi) {
-    const int64_t ri = qi / (2 * nch);
-    const int c = static_cast<int>(qi % nch);
-    const int64_t row = blockIdx.x + ri * gridDim.x;
-    const int64_t off = static_cast<int64_t>(c) * RING_CHUNK;
-    const uint32_t bytes = static_cast<uint32_t>(row_bytes - off < RING_CHUNK ? row_bytes - off : RING_CHUNK);
-    const int b = static_cast<int>(qi % RING);
-    mbar_arrive_expect_tx(full0 + 8u * b, bytes);
-    bulk_copy_g2s(ring0 + b * RING_CHUNK, reinterpret_cast<const uint8_t*>(Z) + row * row_bytes + off, bytes,
-                  full0 + 8u * b);
-    issued = qi + 1;
-  };
-  // bounded wait; after a timeout in this block nobody waits again
-  auto wait_bar = [&](uint32_t bar, uint32_t parity) {
-    if (s_abort) return;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-      if (s_abort) return;
-      if (globaltimer_ns() - t0 > wait_ns) {
-        s_abort = 1;
-        atomicCAS(status, 0, KD_ERR_TIMEOUT);
-        return;
-      }
-    }
-  };
-
-  if (tid == 0) {
-    for (int b = 0; b < RING; ++b) {
-      mbar_init(full0 + 8u * b, 1);
-      mbar_init(empty0 + 8u * b, NW);
-    }
-    s_abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0)
-    for (int64_t qi = 0; qi < RING && qi < total; ++qi) issue(qi);
-
-  int64_t q = 0;  // next sequence element to consume
-  // consume element q: wait for it, run f(group, group index within the row, h) on this
-  // thread's (up to two) 16-byte groups, release the slot, refill it
-  auto consume = [&](auto&& f) {
-    const int b = static_cast<int>(q % RING);
-    const uint32_t par = static_cast<uint32_t>((q / RING) & 1);
-    wait_bar(full0 + 8u * b, par);
-    const int c = static_cast<int>(q % nch);
-    const int64_t left = row_bytes - static_cast<int64_t>(c) * RING_CHUNK;
-    const int ngr = static_cast<int>((left < RING_CHUNK ? left : RING_CHUNK) / 16);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int g = tid + h * CACHE_THREADS;
-      if (g < ngr) f(ld_shared_v4(ring0 + b * RING_CHUNK + g * 16), c * RING_GROUPS + g, h);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8u * b);
-    if (tid == 0 && q + RING < total && !s_abort) {
-      wait_bar(empty0 + 8u * b, par);
-      if (!s_abort) issue(q + RING);
-    }
-    ++q;
-  };
-
   for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
-    const TL* z = Z + row * static_cast<int64_t>(V);
-    // ---------------- pass 1: slot maxima (h = 0 / 1 groups), online softmax normaliser
-    float fslot0 = -INFINITY, fslot1 = -INFINITY;
+    const RV rv{Z + row * static_cast<int64_t>(V), V};
+    const int ng = rv.groups();
+    // ---------------- pass 1: slot maxima, online softmax normaliser
+    float fslot0 = -INFINITY, fslot1 = -INFINITY;  // two disjoint element sets per thread
     float m = -INFINITY, s = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      consume([&](const uint4& r, int, int h) {
-        float f[PV];
-        Tr::unpack(r, f);
+    int it = 0;
+    for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL, ++it) {
+      if (g0 + (CACHE_UNROLL - 1) * CACHE_THREADS < ng) {
+        // all groups present: one rescale check for CACHE_UNROLL * PV logits
+        typename RV::Raw x[CACHE_UNROLL];
+#pragma unroll
+        for (int u = 0; u < CACHE_UNROLL; ++u) x[u] = rv.load(g0 + u * CACHE_THREADS);
+        float f[CACHE_UNROLL * PV];
+#pragma unroll
+        for (int u = 0; u < CACHE_UNROLL; ++u) {
+          float fu[PV];
+          RV::floats(x[u], fu);
+#pragma unroll
+          for (int i = 0; i < PV; ++i) f[u * PV + i] = fu[i];
+        }
         float fmx = f[0];
 #pragma unroll
-        for (int i = 1; i < PV; ++i) fmx = fmaxf(fmx, f[i]);
+        for (int i = 1; i < CACHE_UNROLL * PV; ++i) fmx = fmaxf(fmx, f[i]);
         lse_fold(m, s, fmx, f);
-        if (h) fslot1 = fmaxf(fslot1, fmx);
+        if (it & 1) fslot1 = fmaxf(fslot1, fmx);
         else fslot0 = fmaxf(fslot0, fmx);
-      });
+      } else {
+        for (int u = 0; u < CACHE_UNROLL && g0 + u * CACHE_THREADS < ng; ++u) {
+          float f[PV];
+          RV::floats(rv.load(g0 + u * CACHE_THREADS), f);
+          float fmx = f[0];
+#pragma unroll
+          for (int i = 1; i < PV; ++i) fmx = fmaxf(fmx, f[i]);
+          lse_fold(m, s, fmx, f);
+          if (it & 1) fslot1 = fmaxf(fslot1, fmx);
+          else fslot0 = fmaxf(fslot0, fmx);
+        }
+      }
     }
-    const uint32_t k0 = Tr::fkey(fslot0), k1 = Tr::fkey(fslot1);
-    uint64_t lo, hi;
-    row_stats(m, s, k0, k1, red_m, red_s, red_k, &s_lse, &s_count, &lo, &hi);
-    const uint32_t theta = kth_slot_key(k0, k1, K, lo, hi);
+    if constexpr (VEC) {  // the tail that does not fill a 16-byte vector
+      for (int j = ng * PV + tid; j < V; j += CACHE_THREADS) {
+        const float f[1] = {Tr::value(rv.z[j])};
+        lse_fold(m, s, f[0], f);
+        fslot1 = fmaxf(fslot1, f[0]);
+      }
+    }
+    // slots without elements hold -inf: no larger than any element, so they never raise theta
+    const uint32_t kslot0 = Tr::fkey(fslot0), kslot1 = Tr::fkey(fslot1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+    __syncthreads();  // the previous row's shared state is no longer read
+    if (lane == 0) {
+      red_m[warp] = m;
+      red_s[warp] = s;
+    }
+    if (tid == 0) s_count = 0;
+    __syncthreads();
+    if (warp == 0) {
+      float mm = lane < NW ? red_m[lane] : -INFINITY;
+      float ss = lane < NW ? red_s[lane] : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lse_merge(mm, ss, __shfl_xor_sync(0xffffffffu, mm, o), __shfl_xor_sync(0xffffffffu, ss, o));
+      if (lane == 0) s_lse = mm + log2f(ss) * kLn2;
+    }
+    // ---------------- theta: the K-th largest of the 1024 slot maxima (slots
+    // without elements hold key 0, the smallest key)
+    uint64_t lo = 0, hi = (Tr::KEY_BITS == 32) ? 0xFFFFFFFFull : 0xFFFFull;
+    while (lo < hi) {
+      const uint64_t mid = lo + (hi - lo + 1) / 2;
+      const int c = __syncthreads_count(kslot0 >= mid) + __syncthreads_count(kslot1 >= mid);
+      if (c >= K) lo = mid;
+      else hi = mid - 1;
+    }
+    const uint32_t theta = static_cast<uint32_t>(lo);
+
+    // ---------------- pass 2: candidates with key >= theta, i.e. value >= theta's value
     const float tv = Tr::kvalue(theta);
-    // ---------------- pass 2: candidates with value >= theta's value
-    for (int c = 0; c < nch; ++c) {
-      consume([&](const uint4& r, int g, int) {
-        if (!(Tr::group_max(r) >= tv)) return;  // the common case: no candidate in the group
+    for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL) {
+      typename RV::Raw x[CACHE_UNROLL];
+#pragma unroll
+      for (int u = 0; u < CACHE_UNROLL; ++u)
+        if (g0 + u * CACHE_THREADS < ng) x[u] = rv.load(g0 + u * CACHE_THREADS);
+#pragma unroll
+      for (int u = 0; u < CACHE_UNROLL; ++u) {
+        const int g = g0 + u * CACHE_THREADS;
+        if (g >= ng) break;
+        if constexpr (VEC) {
+          if (!(Tr::group_max(x[u]) >= tv)) continue;  // the common case: no candidate in the group
+        }
         float f[PV];
-        Tr::unpack(r, f);
+        RV::floats(x[u], f);
 #pragma unroll
         for (int i = 0; i < PV; ++i) {
           if (f[i] >= tv) {
@@ -496,16 +298,100 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
               cand[at] = (static_cast<uint64_t>(~Tr::fkey(f[i])) << 32) | static_cast<uint32_t>(g * PV + i);
           }
         }
-      });
+      }
+    }
+    if constexpr (VEC) {
+      for (int j = ng * PV + tid; j < V; j += CACHE_THREADS) {
+        const float f = Tr::value(rv.z[j]);
+        if (f >= tv) {
+          const int at = atomicAdd(&s_count, 1);
+          if (at < CACHE_CAP) cand[at] = (static_cast<uint64_t>(~Tr::fkey(f)) << 32) | static_cast<uint32_t>(j);
+        }
+      }
     }
     __syncthreads();
-    select_and_emit<TL>(z, V, K, s_count, theta, cand, red_i, &s_count, s_lse, idx_out + row * K, p_out + row * K);
-    if (tid == 0 && lse_out) lse_out[row] = s_lse;
-  }
-  // the copies issued last must have landed before the block's shared memory goes away
-  if (tid == 0) {
-    for (int64_t qi = issued - 1; qi >= 0 && qi >= issued - RING; --qi)
-      mbar_wait_quiet(full0 + 8u * static_cast<uint32_t>(qi % RING), static_cast<uint32_t>((qi / RING) & 1), wait_ns);
+    int n = s_count;
+    if (n > CACHE_CAP) {
+      // ---------------- fallback: exact K-th key by binary search, then ordered ties
+      // largest kappa with count(key >= kappa) >= K, searched in [theta, 2^bits - 1]
+      uint64_t lo2 = theta, hi2 = (Tr::KEY_BITS == 32) ? 0xFFFFFFFFull : 0xFFFFull;
+      while (lo2 < hi2) {
+        const uint64_t mid = lo2 + (hi2 - lo2 + 1) / 2;
+        int c = 0;
+        for (int j = tid; j < V; j += CACHE_THREADS) c += static_cast<uint64_t>(Tr::key(rv.z[j])) >= mid;
+        if (block_sum_int(c, red_i) >= K) lo2 = mid;
+        else hi2 = mid - 1;
+      }
+      const uint32_t kappa = static_cast<uint32_t>(lo2);
+      __syncthreads();
+      if (tid == 0) s_count = 0;
+      __syncthreads();
+      for (int j = tid; j < V; j += CACHE_THREADS) {  // fewer than K are strictly above kappa
+        const uint32_t k = Tr::key(rv.z[j]);
+        if (k > kappa) cand[atomicAdd(&s_count, 1)] = (static_cast<uint64_t>(~k) << 32) | static_cast<uint32_t>(j);
+      }
+      __syncthreads();
+      int taken = s_count;
+      // ties at kappa in ascending id order, one block-wide segment at a time
+      for (int base = 0; base < V && taken < K; base += CACHE_THREADS) {
+        const int j = base + tid;
+        const bool tie = j < V && Tr::key(rv.z[j]) == kappa;
+        const unsigned bal = __ballot_sync(0xffffffffu, tie);
+        __syncthreads();
+        if (lane == 0) red_i[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += red_i[w];
+        const int rank_in = before + __popc(bal & ((1u << lane) - 1u));
+        if (tie && taken + rank_in < K)
+          cand[taken + rank_in] = (static_cast<uint64_t>(~kappa) << 32) | static_cast<uint32_t>(j);
+        int total = 0;
+        for (int w = 0; w < NW; ++w) total += red_i[w];
+        taken += total;
+      }
+      n = K;
+      __syncthreads();
+    }
+    // ---------------- order the candidates and emit the top K
+    const float lse = s_lse;
+    if (n <= 2 * CACHE_THREADS) {
+      // rank of each candidate = number of smaller composite keys (all distinct)
+      uint64_t mine[2];
+      int rank[2] = {0, 0};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) mine[h] = (tid + h * CACHE_THREADS < n) ? cand[tid + h * CACHE_THREADS] : ~0ull;
+      if (tid < n) {  // only candidate owners count
+        if (tid + CACHE_THREADS < n) {
+          for (int j = 0; j < n; ++j) {
+            const uint64_t c = cand[j];
+            rank[0] += c < mine[0];
+            rank[1] += c < mine[1];
+          }
+        } else {
+          for (int j = 0; j < n; ++j) rank[0] += cand[j] < mine[0];
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (tid + h * CACHE_THREADS < n && rank[h] < K) {
+          const int id = static_cast<int>(mine[h] & 0xFFFFFFFFu);
+          idx_out[row * K + rank[h]] = id;
+          p_out[row * K + rank[h]] = ex2((Tr::value(rv.z[id]) - lse) * kLog2e);
+        }
+      }
+    } else {
+      int n_pad = 1;
+      while (n_pad < n) n_pad <<= 1;
+      for (int i = n + tid; i < n_pad; i += CACHE_THREADS) cand[i] = ~0ull;
+      __syncthreads();
+      block_bitonic_sort_u64(cand, n_pad);
+      for (int k = tid; k < K; k += CACHE_THREADS) {
+        const int id = static_cast<int>(cand[k] & 0xFFFFFFFFu);
+        idx_out[row * K + k] = id;
+        p_out[row * K + k] = ex2((Tr::value(rv.z[id]) - lse) * kLog2e);
+      }
+    }
+    if (tid == 0 && lse_out) lse_out[row] = lse;
   }
 }
 

@@ -104,14 +104,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-// Untiled bulk copy global -> this CTA's shared memory, completion on `bar`
-// (both addresses 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* tm, int x,
                                                  int y, uint32_t bar, uint64_t policy) {
   asm volatile(

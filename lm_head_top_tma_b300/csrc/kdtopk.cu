@@ -527,52 +527,38 @@ kd_status kd_topk_kl_fused_step_norecompute(const void* H, const void* W, const 
 }
 
 kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, int V, int K, int32_t* idx,
-                              float* p, float* lse, void* workspace, size_t ws_bytes, void* stream) {
-  if (!logits || !idx || !p || !workspace || T < 1 || V < 1 || K < 1 || K > V) return KD_ERR_INVALID_ARG;
+                              float* p, float* lse, void* stream) {
+  if (!logits || !idx || !p || T < 1 || V < 1 || K < 1 || K > V) return KD_ERR_INVALID_ARG;
   if (K > 1024) return KD_ERR_UNSUPPORTED;
-  if (ws_bytes < 256 || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KD_ERR_WORKSPACE;
   const uintptr_t need = logits_bf16 ? 1u : 3u;
   if ((reinterpret_cast<uintptr_t>(logits) & need) || (reinterpret_cast<uintptr_t>(idx) & 3u) ||
       (reinterpret_cast<uintptr_t>(p) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return KD_ERR_UNSUPPORTED;
   if (!device_supported()) return KD_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int* status = static_cast<int*>(workspace);
-  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
-  // rows that start on 16-byte boundaries stream through the shared-memory ring
-  const bool stream_rows =
-      (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (int64_t(V) * (logits_bf16 ? 2 : 4)) % 16 == 0;
+  // 16-byte loads when every row starts on a 16-byte boundary
+  const bool vec = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (int64_t(V) * (logits_bf16 ? 2 : 4)) % 16 == 0;
   const int sms = current_sm_count();
   const int slot = prof_begin(KD_K_OTHER, st);
   cudaError_t e = cudaSuccess;
-  auto blocks_for = [&](const void* kern, size_t dyn) {
+  auto run_kernel = [&](auto kern, const auto* z) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CACHE_THREADS, dyn) != cudaSuccess || per_sm < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CACHE_THREADS, 0) != cudaSuccess || per_sm < 1) {
       cudaGetLastError();
       per_sm = 1;
     }
-    return static_cast<int>(std::min<int64_t>(T, int64_t(per_sm) * sms));
-  };
-  auto run_stream = [&](auto kern, const auto* z) {
-    constexpr size_t dyn = size_t(RING) * RING_CHUNK;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
-    if (e != cudaSuccess) return;
-    kern<<<blocks_for(reinterpret_cast<const void*>(kern), dyn), CACHE_THREADS, dyn, st>>>(z, T, V, K, idx, p, lse,
-                                                                                          status, wait_limit_ns());
-    e = cudaGetLastError();
-  };
-  auto run_plain = [&](auto kern, const auto* z) {
-    kern<<<blocks_for(reinterpret_cast<const void*>(kern), 0), CACHE_THREADS, 0, st>>>(z, T, V, K, idx, p, lse);
+    const int blocks = static_cast<int>(std::min<int64_t>(T, int64_t(per_sm) * sms));
+    kern<<<blocks, CACHE_THREADS, 0, st>>>(z, T, V, K, idx, p, lse);
     e = cudaGetLastError();
   };
   if (logits_bf16) {
     const auto* z = static_cast<const __nv_bfloat16*>(logits);
-    if (stream_rows) run_stream(kd_topk_cache_stream_kernel<__nv_bfloat16>, z);
-    else run_plain(kd_topk_cache_kernel<__nv_bfloat16>, z);
+    if (vec) run_kernel(kd_topk_cache_kernel<__nv_bfloat16, true>, z);
+    else run_kernel(kd_topk_cache_kernel<__nv_bfloat16, false>, z);
   } else {
     const auto* z = static_cast<const float*>(logits);
-    if (stream_rows) run_stream(kd_topk_cache_stream_kernel<float>, z);
-    else run_plain(kd_topk_cache_kernel<float>, z);
+    if (vec) run_kernel(kd_topk_cache_kernel<float, true>, z);
+    else run_kernel(kd_topk_cache_kernel<float, false>, z);
   }
   prof_end(slot, st);
   return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
