@@ -35,13 +35,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); peak bytes vs T"
 
-# DRAM traffic of the dominant kernel from an ncu capture (profiles/gemm_traffic_longctx_chunk2048.md);
-# reported only while the kernel sources still hash to what was captured.  dW GEMM (pair form), one
-# launch per group of two 2048-row chunks of the long-context head: the first group stores dW
-# (3.120 GB), every later group reduce-adds into it (4.289 GB); bench lines weight the two by the
-# launch mix.
-TRAFFIC = {"kernel": "gemm_dw", "workload": "longctx", "store_bytes": 1574785792 + 1544741120,
-           "accumulate_bytes": 2751875840 + 1536651264, "src_sha": "536786b56684b548"}
+# DRAM traffic per launch of the kernels that can dominate the step, from ncu
+# captures (profiles/gemm_traffic_longctx_chunk2048.md); reported only while the
+# kernel sources still hash to what was captured.  gemm_dw: one launch per group
+# of two 2048-row chunks, the first group of a step stores dW ("first"), the
+# others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
+# chunk's forward.
+TRAFFIC = {"workload": "longctx", "src_sha": None, "kinds": {}}
 KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300/csrc/kd_ptx.cuh",
                   "lm_head_top_tma_b300/csrc/kdtopk.cu"]
 
@@ -381,18 +381,26 @@ def run_kdtopk(args):
     flops_6 = 6.0 * T * V * d
     peaks = load_peaks()
     # dominant kernel: the kind with the largest total time inside the timed region.
-    # Each chunk GEMM kind does 2 T V d flops per step in total; a dW launch covers
-    # a group of chunks, so per-launch work = 2 T V d / (its launches per step).
-    gemm_kinds = ("logits_fwd", "logits_g", "gemm_dh", "gemm_dw")
+    # Per-launch work: a chunk's logits GEMM (forward or G) and its dH GEMM do
+    # 2 C V d flops; the merged launch of one chunk's G and the next chunk's
+    # forward does 4 C V d; a dW launch covers a group of chunks, 2 T V d per
+    # step over its launches.
     dom = max(prof, key=lambda k: prof[k][0])
     dom_ms, dom_n = prof[dom]
-    per_launch_flops = 2.0 * T * V * d / (dom_n / args.steps) if (dom in gemm_kinds and dom_n) else None
+    Cc = min(C, T)
+    launch_flops = {"logits_fwd": 2.0 * Cc * V * d, "logits_g": 2.0 * Cc * V * d, "logits_gf": 4.0 * Cc * V * d,
+                    "gemm_dh": 2.0 * Cc * V * d}
+    if dom == "gemm_dw" and dom_n:
+        per_launch_flops = 2.0 * T * V * d / (dom_n / args.steps)
+    else:
+        per_launch_flops = launch_flops.get(dom)
     achieved = per_launch_flops / (dom_ms / dom_n / 1e3) / 1e12 if per_launch_flops and dom_n else None
     traffic = None
-    if (TRAFFIC["kernel"] == dom and TRAFFIC["workload"] == wl.name and C == get_workload(wl.name).chunk
+    tk = TRAFFIC["kinds"].get(dom)
+    if (tk and TRAFFIC["workload"] == wl.name and C == get_workload(wl.name).chunk
             and TRAFFIC["src_sha"] == kernel_src_sha() and dom_n):
-        n_launch = dom_n // args.steps  # the first launch of a step stores dW, the rest accumulate
-        traffic = (TRAFFIC["store_bytes"] + (n_launch - 1) * TRAFFIC["accumulate_bytes"]) / n_launch
+        n_launch = dom_n // args.steps  # per step: one "first" launch, the others "rest"
+        traffic = (tk["first"] + (n_launch - 1) * tk["rest"]) / n_launch
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sustained"],
                 "unit": "TFLOP/s", "frac": (achieved / peaks["bf16_sustained"]) if achieved else None,
                 "traffic": traffic, "peak_kind": f"bf16 sustained ({peaks['source']})",

@@ -124,7 +124,11 @@ KD_API kd_status kd_topk_kl_backward(const void* H, const void* W, const int32_t
 /*
  * Forward and backward in one pass over the chunks: per chunk the logits are
  * computed once for the normaliser and once more for G.  Outputs as above
- * (loss_rows may be NULL).
+ * (loss_rows may be NULL).  The loop is pipelined by one chunk: chunk c's G
+ * GEMM and chunk c+1's forward GEMM run as one launch over both chunks' rows,
+ * sharing every W tile (results are those of separate launches, bit for bit;
+ * environment variable KD_MERGE_LOGITS=0, read once per process, keeps them
+ * apart).
  */
 KD_API kd_status kd_topk_kl_fused_step(const void* H, const void* W, const int32_t* idx, const float* p,
                                 int64_t T, int d, int V, int K, int chunk,
@@ -243,10 +247,10 @@ KD_API kd_status kd_debug_wait_timeout(int wait_limit_ms, int cta_pair, void* wo
  * kd_profile_read synchronises, fills per-kind totals and launch counts for
  * up to `n` kinds and returns the number of kinds (KD_PROF_KINDS).
  */
-#define KD_PROF_KINDS 9
+#define KD_PROF_KINDS 10
 enum { KD_K_PREP = 0, KD_K_LOGITS_FWD = 1, KD_K_COMBINE = 2, KD_K_LOGITS_G = 3,
        KD_K_GEMM_DH = 4, KD_K_DH_REDUCE = 5, KD_K_GEMM_DW = 6, KD_K_OTHER = 7,
-       KD_K_G_FROM_E = 8 };
+       KD_K_G_FROM_E = 8, KD_K_LOGITS_GF = 9 };
 KD_API kd_status kd_profile_enable(int on);
 KD_API int kd_profile_read(double* ms_total, int64_t* launches, int n, int reset);
 KD_API const char* kd_profile_kind_name(int kind);

@@ -22,7 +22,7 @@ KD_WS_FORWARD = 1
 KD_WS_BACKWARD = 2
 KD_WS_FUSED = 3
 
-KD_PROF_KINDS = 9
+KD_PROF_KINDS = 10
 KD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _c_p = ctypes.c_void_p

@@ -36,6 +36,9 @@
 //            TMA into the chunk's [chunk, V] operand buffer, where a later
 //            elementwise pass turns them into G once lse is known (the fused
 //            step without the backward recompute).
+//   EPI_GF   two adjacent chunks in one launch: row tiles below m_split are
+//            chunk c's G tiles (EPI_G), the others chunk c+1's forward tiles
+//            (EPI_FWD); both halves share every W tile through L2.
 //   EPI_F32  fp32 tile, scaled, staged through shared memory (128 x 32 slices,
 //            128-byte swizzle) and written by TMA: a plain store, or a TMA
 //            reduce-add so that L2 performs the read-modify-write of dW while
@@ -66,7 +69,7 @@ constexpr int OUT_STAGING_BYTES = 2 * OUT_SLICE_BYTES;
 constexpr int EPI_WARPS = 4;
 constexpr uint32_t EPI_BAR_ID = 1;  // named barrier of the epilogue warps
 
-enum Epi { EPI_FWD = 0, EPI_G = 1, EPI_F32 = 2, EPI_FWD_E = 3 };
+enum Epi { EPI_FWD = 0, EPI_G = 1, EPI_F32 = 2, EPI_FWD_E = 3, EPI_GF = 4 };
 
 __host__ __device__ constexpr int staging_bytes(int epi) { return epi == EPI_FWD ? 0 : OUT_STAGING_BYTES; }
 
@@ -115,6 +118,11 @@ struct GemmParams {
   int out_row0, split_rows;
   int reduce_add;
   float scale;
+  // EPI_GF: row tiles m >= m_split are the forward of the next chunk, whose
+  // H rows start at a_mn0_2, with rows_valid2 rows and sorted cache sidx2/sp2
+  int m_split, a_mn0_2, rows_valid2;
+  const int32_t* sidx2;
+  const float* sp2;
 };
 
 __device__ __forceinline__ void decode_tile(const GemmParams& P, int tile, int& m, int& n, int& s) {
@@ -232,7 +240,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         decode_tile(P, tile, m, n, s);
         const int kb0 = s * P.kb_per_split;
         const int kb1 = min(P.kb_total, kb0 + P.kb_per_split);
-        const int a_row = P.a_mn0 + m * Cfg::TILE_M + static_cast<int>(rank) * BM;
+        const bool next_part = EPI == EPI_GF && m >= P.m_split;  // the next chunk's forward rows
+        const int a_row = (next_part ? P.a_mn0_2 + (m - P.m_split) * Cfg::TILE_M : P.a_mn0 + m * Cfg::TILE_M) +
+                          static_cast<int>(rank) * BM;
         const int b_row = P.b_mn0 + n * BN + static_cast<int>(rank) * Cfg::B_ROWS;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, wc)) {
@@ -343,7 +353,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int acc = local & 1;
       const uint32_t acc_par = (local >> 1) & 1;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      const int row0 = m * Cfg::TILE_M + static_cast<int>(rank) * BM;  // first row of D this CTA holds
+      // which epilogue this tile runs: the forward statistics or G (runtime only for EPI_GF)
+      const bool next_part = EPI == EPI_GF && m >= P.m_split;
+      const bool is_fwd = EPI == EPI_FWD || next_part;
+      const int mm = next_part ? m - P.m_split : m;                         // tile row within its chunk
+      const int row0 = mm * Cfg::TILE_M + static_cast<int>(rank) * BM;  // first row of D this CTA holds
       const int r = row0 + row_in_tile;
 
       // per-row set-up, overlapping the mainloop of this tile
@@ -352,11 +366,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int cur = 0, cid = INT_MAX;
       float cp = 0.f, Mr = 0.f, nl2 = 0.f;
       bool rv = false;
-      if constexpr (EPI == EPI_FWD || EPI == EPI_G || EPI == EPI_FWD_E) {
-        rv = r < P.rows_valid;
+      if constexpr (EPI == EPI_FWD || EPI == EPI_G || EPI == EPI_FWD_E || EPI == EPI_GF) {
+        rv = r < (next_part ? P.rows_valid2 : P.rows_valid);
         const int n0 = n * BN;
-        ids = P.sidx + static_cast<size_t>(r) * P.K;
-        ps = P.sp + static_cast<size_t>(r) * P.K;
+        ids = (next_part ? P.sidx2 : P.sidx) + static_cast<size_t>(r) * P.K;
+        ps = (next_part ? P.sp2 : P.sp) + static_cast<size_t>(r) * P.K;
         int lo = 0, hi = P.K;  // first sorted position with id >= n0
         while (lo < hi) {
           const int mid = (lo + hi) >> 1;
@@ -368,8 +382,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           cid = __ldg(ids + cur);
           cp = __ldg(ps + cur);
         }
-        if constexpr (EPI == EPI_G) {
-          if (rv) {
+        if constexpr (EPI == EPI_G || EPI == EPI_GF) {
+          if (!is_fwd && rv) {
             Mr = __ldg(P.rowM + r);
             nl2 = -__ldg(P.lse + r) * kLog2e;
           }
@@ -405,7 +419,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         float v[32];
         tmem_ld32(taddr + c * 32, v);
         const int col0 = n * BN + c * 32;
-        if constexpr (EPI == EPI_FWD) {
+        if (EPI == EPI_FWD || (EPI == EPI_GF && is_fwd)) {
           if (col0 < P.V) {
             const int nv = min(32, P.V - col0);
             float wm = -INFINITY;
@@ -434,7 +448,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               cp = cur < P.K ? __ldg(ps + cur) : 0.f;
             }
           }
-        } else if constexpr (EPI == EPI_G) {
+        } else if (EPI == EPI_G || EPI == EPI_GF) {
           // two 32-column windows fill one 128 x 64 bf16 slice of the staging buffer
           const uint32_t buf = staging_base + (slice & 1u) * OUT_SLICE_BYTES;
           if ((c & 1) == 0) {
@@ -462,7 +476,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             ++slice;
           }
-        } else if constexpr (EPI == EPI_FWD_E) {
+        } else if (EPI == EPI_FWD_E) {
           const uint32_t buf = staging_base + (slice & 1u) * OUT_SLICE_BYTES;
           if ((c & 1) == 0) {
             if (out_leader) bulk_wait_read1();  // the store that last read `buf` is done with it
@@ -532,8 +546,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(tempty0 + 8u * acc, 0));
         else mbar_arrive(tempty0 + 8u * acc);
       }
-      if constexpr (EPI == EPI_FWD || EPI == EPI_FWD_E) {
-        if (rv) {
+      if constexpr (EPI == EPI_FWD || EPI == EPI_FWD_E || EPI == EPI_GF) {
+        if (rv && (EPI != EPI_GF || is_fwd)) {
           const size_t o = static_cast<size_t>(n) * P.ld_part + r;
           P.part_m[o] = run_m;
           P.part_s[o] = run_s;

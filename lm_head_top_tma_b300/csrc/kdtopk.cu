@@ -128,6 +128,16 @@ bool pair_enabled() {
   return v;
 }
 
+// The recompute fused step runs chunk c's G GEMM and chunk c+1's forward GEMM
+// as one launch; KD_MERGE_LOGITS=0 (read once per process) keeps them apart.
+bool merge_enabled() {
+  static bool v = [] {
+    const char* e = std::getenv("KD_MERGE_LOGITS");
+    return !(e && std::atoi(e) == 0);
+  }();
+  return v;
+}
+
 uint64_t wait_limit_ns() {
   static uint64_t v = [] {
     const char* e = std::getenv("KD_WAIT_LIMIT_MS");
@@ -167,6 +177,8 @@ void prof_end(int slot, cudaStream_t st) {
 struct Plan {
   int64_t T;
   int d, V, K, C, Cpad, Kpad, nt, S, kbps_dh, nchunks;
+  int prep_bufs;  // sorted-cache buffers: 2 when one chunk's backward overlaps the next chunk's forward
+  size_t prep_stride;  // bytes between them
   bool pair;     // chunk GEMMs run as CTA pairs (tiles of 256 rows)
   int tile_m;    // rows per GEMM tile: 256 for pairs, 128 otherwise
   int dw_group;  // chunks whose G rows one dW GEMM consumes (K = dw_group * C)
@@ -226,10 +238,15 @@ kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* p
     return at;
   };
   p.off_status = take(256);  // int status + double loss accumulator
+  // prep outputs (sorted ids, their p, M_t, E_t); the fused step keeps two sets
+  p.prep_bufs = ((what & KD_WS_FUSED) == KD_WS_FUSED) ? 2 : 1;
+  const size_t prep_start = o;
   p.off_sidx = take(size_t(p.Cpad) * K * 4);
   p.off_sp = take(size_t(p.Cpad) * K * 4);
   p.off_M = take(size_t(p.Cpad) * 4);
   p.off_E = take(size_t(p.Cpad) * 4);
+  p.prep_stride = o - prep_start;
+  if (p.prep_bufs == 2) o += p.prep_stride;
   p.off_pm = p.off_ps = p.off_pz = p.off_Lrow = 0;
   p.off_G = p.off_dhp = 0;
   if (what & KD_WS_FORWARD) {
@@ -339,10 +356,6 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(w8 + pl.off_status);
   double* loss_acc = reinterpret_cast<double*>(w8 + pl.off_status + 8);
-  int32_t* sidx = reinterpret_cast<int32_t*>(w8 + pl.off_sidx);
-  float* sp = reinterpret_cast<float*>(w8 + pl.off_sp);
-  float* rowM = reinterpret_cast<float*>(w8 + pl.off_M);
-  float* rowE = reinterpret_cast<float*>(w8 + pl.off_E);
   float* pm = reinterpret_cast<float*>(w8 + pl.off_pm);
   float* ps = reinterpret_cast<float*>(w8 + pl.off_ps);
   float* ppz = reinterpret_cast<float*>(w8 + pl.off_pz);
@@ -376,110 +389,153 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
     return KD_ERR_CUDA;
 
   const bool keep = (mode & MODE_KEEP) != 0;
-  for (int c = 0; c < pl.nchunks; ++c) {
-    const int64_t t0 = int64_t(c) * pl.C;
-    const int rows = static_cast<int>(std::min<int64_t>(pl.C, T - t0));
-    const int gslot = c % pl.dw_group;  // this chunk's G rows: [gslot * Cpad, +Cpad)
-    __nv_bfloat16* Gc = G + size_t(gslot) * pl.Cpad * pl.ldg;
-    cudaError_t e;
-    // -------- prep
-    {
-      const int slot = prof_begin(KD_K_PREP, st);
-      kd_prep_kernel<<<static_cast<unsigned>(ceil_div(pl.Cpad, PREP_WARPS)), PREP_WARPS * 32, prep_smem, st>>>(
-          idx + t0 * K, p + t0 * K, rows, pl.Cpad, K, pl.Kpad, V, sidx, sp, rowM, rowE, status);
-      e = cudaGetLastError();
-      prof_end(slot, st);
-      if (e != cudaSuccess) return KD_ERR_CUDA;
-    }
+  const int kb_d = static_cast<int>(ceil_div(d, BK));
+  auto t0_of = [&](int c) { return int64_t(c) * pl.C; };
+  auto rows_of = [&](int c) { return static_cast<int>(std::min<int64_t>(pl.C, T - t0_of(c))); };
+  auto gslot_of = [&](int c) { return c % pl.dw_group; };  // chunk c's G rows: [gslot * Cpad, +Cpad)
+  // the sorted cache of chunk c lives in prep buffer c % prep_bufs
+  auto pbuf = [&](int c, size_t off) { return w8 + off + size_t(c % pl.prep_bufs) * pl.prep_stride; };
+  auto sidx_of = [&](int c) { return reinterpret_cast<int32_t*>(pbuf(c, pl.off_sidx)); };
+  auto sp_of = [&](int c) { return reinterpret_cast<float*>(pbuf(c, pl.off_sp)); };
+  auto rowM_of = [&](int c) { return reinterpret_cast<float*>(pbuf(c, pl.off_M)); };
+  auto rowE_of = [&](int c) { return reinterpret_cast<float*>(pbuf(c, pl.off_E)); };
+  auto logits_params = [&](int c) {
     GemmParams L = base_params(status);
     L.num_m = pl.Cpad / pl.tile_m;
     L.num_n = pl.nt;
-    L.kb_total = L.kb_per_split = static_cast<int>(ceil_div(d, BK));
-    L.a_mn0 = static_cast<int>(t0);
-    L.rows_valid = rows;
+    L.kb_total = L.kb_per_split = kb_d;
+    L.a_mn0 = static_cast<int>(t0_of(c));
+    L.rows_valid = rows_of(c);
     L.V = V;
     L.K = K;
-    L.sidx = sidx;
-    L.sp = sp;
-    // -------- forward: lse, loss
-    if (mode & MODE_FWD) {
-      GemmParams P = L;
-      P.part_m = pm;
-      P.part_s = ps;
-      P.part_pz = ppz;
-      P.ld_part = pl.Cpad;
-      if (keep) {
-        P.out_row0 = gslot * pl.Cpad;
-        if (launch_gemm_any<EPI_FWD_E, false, false>(pr, KD_K_LOGITS_FWD, tmH_k, tmW_k, tmG_k, P, sms, st) !=
-            cudaSuccess)
-          return KD_ERR_CUDA;
-      } else if (launch_gemm_any<EPI_FWD, false, false>(pr, KD_K_LOGITS_FWD, tmH_k, tmW_k, tmH_k, P, sms, st) !=
-                 cudaSuccess) {
-        return KD_ERR_CUDA;
-      }
-      const int slot = prof_begin(KD_K_COMBINE, st);
-      kd_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, 32)), COMBINE_WARPS * 32, 0, st>>>(
-          pm, ps, ppz, pl.nt, pl.Cpad, rows, rowM, rowE, lse + t0, loss_rows ? loss_rows + t0 : nullptr, Lrow);
-      kd_loss_reduce_kernel<<<1, 1024, 0, st>>>(Lrow, rows, loss_acc, c == 0 ? 1 : 0,
-                                                c == pl.nchunks - 1 ? loss : nullptr);
-      e = cudaGetLastError();
-      prof_end(slot, st);
-      if (e != cudaSuccess) return KD_ERR_CUDA;
-      if (keep) {  // G from the kept exponentials, in place, now that lse is known
-        const int gs = prof_begin(KD_K_G_FROM_E, st);
-        kd_g_from_e_kernel<<<static_cast<unsigned>(rows), GPASS_THREADS, 0, st>>>(Gc, pl.ldg, rows, V, K, sidx, sp,
-                                                                               rowM, lse + t0, pm, pl.Cpad);
-        e = cudaGetLastError();
-        prof_end(gs, st);
-        if (e != cudaSuccess) return KD_ERR_CUDA;
-      }
-    }
-    // -------- backward: G, dH, dW
-    if (mode & MODE_BWD) {
-      if (!keep) {
-        GemmParams P = L;
-        P.out_row0 = gslot * pl.Cpad;
-        P.rowM = rowM;
-        P.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0;
-        if (launch_gemm_any<EPI_G, false, false>(pr, KD_K_LOGITS_G, tmH_k, tmW_k, tmG_k, P, sms, st) !=
-            cudaSuccess)
-          return KD_ERR_CUDA;
-      }
+    L.sidx = sidx_of(c);
+    L.sp = sp_of(c);
+    L.part_m = pm;
+    L.part_s = ps;
+    L.part_pz = ppz;
+    L.ld_part = pl.Cpad;
+    L.out_row0 = gslot_of(c) * pl.Cpad;
+    L.rowM = rowM_of(c);
+    L.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0_of(c);
+    return L;
+  };
+  auto check = [&](cudaError_t e) { return e == cudaSuccess; };
 
-      GemmParams Q = base_params(status);  // dH partials = G W, split over V
-      Q.num_m = pl.Cpad / pl.tile_m;
-      Q.num_n = static_cast<int>(ceil_div(d, BN));
-      Q.num_s = pl.S;
-      Q.kb_total = static_cast<int>(ceil_div(V, BK));
-      Q.kb_per_split = pl.kbps_dh;
-      Q.split_rows = pl.Cpad;
-      Q.a_mn0 = gslot * pl.Cpad;
-      if (launch_gemm_any<EPI_F32, false, true>(pr, KD_K_GEMM_DH, tmG_k, tmW_mn, tmDhp, Q, sms, st) != cudaSuccess)
+  // ---- the steps of one chunk
+  auto prep = [&](int c) {
+    const int slot = prof_begin(KD_K_PREP, st);
+    kd_prep_kernel<<<static_cast<unsigned>(ceil_div(pl.Cpad, PREP_WARPS)), PREP_WARPS * 32, prep_smem, st>>>(
+        idx + t0_of(c) * K, p + t0_of(c) * K, rows_of(c), pl.Cpad, K, pl.Kpad, V, sidx_of(c), sp_of(c), rowM_of(c),
+        rowE_of(c), status);
+    const cudaError_t e = cudaGetLastError();
+    prof_end(slot, st);
+    return check(e);
+  };
+  auto forward_gemm = [&](int c) {
+    const GemmParams P = logits_params(c);
+    if (keep) return check(launch_gemm_any<EPI_FWD_E, false, false>(pr, KD_K_LOGITS_FWD, tmH_k, tmW_k, tmG_k, P, sms, st));
+    return check(launch_gemm_any<EPI_FWD, false, false>(pr, KD_K_LOGITS_FWD, tmH_k, tmW_k, tmH_k, P, sms, st));
+  };
+  auto combine = [&](int c) {
+    const int rows = rows_of(c);
+    const int slot = prof_begin(KD_K_COMBINE, st);
+    kd_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, 32)), COMBINE_WARPS * 32, 0, st>>>(
+        pm, ps, ppz, pl.nt, pl.Cpad, rows, rowM_of(c), rowE_of(c), lse + t0_of(c),
+        loss_rows ? loss_rows + t0_of(c) : nullptr, Lrow);
+    kd_loss_reduce_kernel<<<1, 1024, 0, st>>>(Lrow, rows, loss_acc, c == 0 ? 1 : 0,
+                                              c == pl.nchunks - 1 ? loss : nullptr);
+    cudaError_t e = cudaGetLastError();
+    prof_end(slot, st);
+    if (e == cudaSuccess && keep) {  // G from the kept exponentials, in place, now that lse is known
+      const int gs = prof_begin(KD_K_G_FROM_E, st);
+      kd_g_from_e_kernel<<<static_cast<unsigned>(rows), GPASS_THREADS, 0, st>>>(
+          G + size_t(gslot_of(c)) * pl.Cpad * pl.ldg, pl.ldg, rows, V, K, sidx_of(c), sp_of(c), rowM_of(c),
+          lse + t0_of(c), pm, pl.Cpad);
+      e = cudaGetLastError();
+      prof_end(gs, st);
+    }
+    return check(e);
+  };
+  auto g_gemm = [&](int c) {
+    const GemmParams P = logits_params(c);
+    return check(launch_gemm_any<EPI_G, false, false>(pr, KD_K_LOGITS_G, tmH_k, tmW_k, tmG_k, P, sms, st));
+  };
+  // chunk c's G and chunk c+1's forward in one launch: both halves share every W tile
+  auto g_and_next_forward = [&](int c) {
+    GemmParams P = logits_params(c);
+    const GemmParams F = logits_params(c + 1);
+    P.m_split = P.num_m;
+    P.num_m = 2 * P.num_m;
+    P.a_mn0_2 = F.a_mn0;
+    P.rows_valid2 = F.rows_valid;
+    P.sidx2 = F.sidx;
+    P.sp2 = F.sp;
+    return check(launch_gemm_any<EPI_GF, false, false>(pr, KD_K_LOGITS_GF, tmH_k, tmW_k, tmG_k, P, sms, st));
+  };
+  auto dh_and_dw = [&](int c) {
+    const int gslot = gslot_of(c);
+    GemmParams Q = base_params(status);  // dH partials = G W, split over V
+    Q.num_m = pl.Cpad / pl.tile_m;
+    Q.num_n = static_cast<int>(ceil_div(d, BN));
+    Q.num_s = pl.S;
+    Q.kb_total = static_cast<int>(ceil_div(V, BK));
+    Q.kb_per_split = pl.kbps_dh;
+    Q.split_rows = pl.Cpad;
+    Q.a_mn0 = gslot * pl.Cpad;
+    if (!check(launch_gemm_any<EPI_F32, false, true>(pr, KD_K_GEMM_DH, tmG_k, tmW_mn, tmDhp, Q, sms, st)))
+      return false;
+    {
+      const int64_t n4 = int64_t(rows_of(c)) * d / 4;
+      const int slot = prof_begin(KD_K_DH_REDUCE, st);
+      kd_dh_reduce_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(n4, 256), 4L * sms)), 256, 0, st>>>(
+          reinterpret_cast<const float4*>(dhp), pl.S, int64_t(pl.Cpad) * d / 4, n4, dloss,
+          reinterpret_cast<float4*>(dH + t0_of(c) * d));
+      const cudaError_t e = cudaGetLastError();
+      prof_end(slot, st);
+      if (e != cudaSuccess) return false;
+    }
+    if (gslot == pl.dw_group - 1 || c == pl.nchunks - 1) {
+      // dW (+)= G^T H over the group's chunks, fp32; the first group stores, the rest add in L2
+      const int first = c - gslot;
+      GemmParams R = base_params(status);
+      R.num_m = static_cast<int>(ceil_div(V, pl.tile_m));
+      R.num_n = static_cast<int>(ceil_div(d, BN));
+      R.m_fast = 0;
+      R.kb_total = R.kb_per_split = (gslot + 1) * pl.Cpad / BK;
+      R.b_k0 = static_cast<int>(int64_t(first) * pl.C);
+      R.reduce_add = (first == 0 && !accumulate) ? 0 : 1;
+      R.scale = dloss;
+      if (!check(launch_gemm_any<EPI_F32, true, true>(pr, KD_K_GEMM_DW, tmG_mn, tmH_mn, tmDW, R, sms, st)))
+        return false;
+    }
+    return true;
+  };
+
+  const bool fused = (mode & MODE_FWD) && (mode & MODE_BWD);
+  if (fused && !keep && pl.prep_bufs == 2 && pl.nchunks > 1 && merge_enabled()) {
+    // recompute path, software-pipelined by one chunk: after chunk c's forward and
+    // combine, chunk c's G GEMM runs together with chunk c+1's forward GEMM
+    if (!prep(0) || !forward_gemm(0) || !combine(0)) return KD_ERR_CUDA;
+    for (int c = 0; c < pl.nchunks; ++c) {
+      const bool more = c + 1 < pl.nchunks;
+      if (more) {
+        if (!prep(c + 1) || !g_and_next_forward(c)) return KD_ERR_CUDA;
+      } else if (!g_gemm(c)) {
         return KD_ERR_CUDA;
-      {
-        const int64_t n4 = int64_t(rows) * d / 4;
-        const int slot = prof_begin(KD_K_DH_REDUCE, st);
-        kd_dh_reduce_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(n4, 256), 4L * sms)), 256, 0, st>>>(
-            reinterpret_cast<const float4*>(dhp), pl.S, int64_t(pl.Cpad) * d / 4, n4, dloss,
-            reinterpret_cast<float4*>(dH + t0 * d));
-        e = cudaGetLastError();
-        prof_end(slot, st);
-        if (e != cudaSuccess) return KD_ERR_CUDA;
       }
-      if (gslot == pl.dw_group - 1 || c == pl.nchunks - 1) {
-        // dW (+)= G^T H over the group's chunks, fp32; the first group stores, the rest add in L2
-        const int first = c - gslot;
-        GemmParams R = base_params(status);
-        R.num_m = static_cast<int>(ceil_div(V, pl.tile_m));
-        R.num_n = static_cast<int>(ceil_div(d, BN));
-        R.m_fast = 0;
-        R.kb_total = R.kb_per_split = (gslot + 1) * pl.Cpad / BK;
-        R.b_k0 = static_cast<int>(int64_t(first) * pl.C);
-        R.reduce_add = (first == 0 && !accumulate) ? 0 : 1;
-        R.scale = dloss;
-        if (launch_gemm_any<EPI_F32, true, true>(pr, KD_K_GEMM_DW, tmG_mn, tmH_mn, tmDW, R, sms, st) != cudaSuccess)
-          return KD_ERR_CUDA;
-      }
+      if (!dh_and_dw(c)) return KD_ERR_CUDA;
+      if (more && !combine(c + 1)) return KD_ERR_CUDA;
+    }
+    return KD_OK;
+  }
+  for (int c = 0; c < pl.nchunks; ++c) {
+    if (!prep(c)) return KD_ERR_CUDA;
+    if (mode & MODE_FWD) {
+      if (!forward_gemm(c) || !combine(c)) return KD_ERR_CUDA;
+    }
+    if (mode & MODE_BWD) {
+      if (!keep && !g_gemm(c)) return KD_ERR_CUDA;
+      if (!dh_and_dw(c)) return KD_ERR_CUDA;
     }
   }
   return KD_OK;
@@ -679,8 +735,8 @@ int kd_profile_read(double* ms_total, int64_t* launches, int n, int reset) {
 }
 
 const char* kd_profile_kind_name(int kind) {
-  static const char* names[KD_PROF_KINDS] = {"prep",    "logits_fwd", "combine", "logits_g", "gemm_dh",
-                                             "dh_reduce", "gemm_dw",   "other",   "g_from_e"};
+  static const char* names[KD_PROF_KINDS] = {"prep",      "logits_fwd", "combine", "logits_g", "gemm_dh",
+                                             "dh_reduce", "gemm_dw",    "other",   "g_from_e", "logits_gf"};
   return (kind >= 0 && kind < KD_PROF_KINDS) ? names[kind] : "unknown";
 }
 
