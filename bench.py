@@ -41,7 +41,10 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 # of two 2048-row chunks, the first group of a step stores dW ("first"), the
 # others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
 # chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": None, "kinds": {}}
+TRAFFIC = {"workload": "longctx", "src_sha": "3b5c948abd4840a7", "kinds": {
+    "gemm_dw": {"first": 1452616704 + 1545390336, "rest": 2782197760 + 1538707200},
+    "logits_gf": {"first": 893756416 + 523619840, "rest": 893756416 + 523619840},
+}}
 KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300/csrc/kd_ptx.cuh",
                   "lm_head_top_tma_b300/csrc/kdtopk.cu"]
 
