@@ -20,6 +20,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -287,17 +288,17 @@ cudaError_t launch_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& tb, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // pairs that can be resident at once (clusters sit within one GPC), asked once per kernel
-    static int resident = 0;
-    if (resident == 0) {
+    static std::atomic<int> resident{0};
+    int res = resident.load(std::memory_order_relaxed);
+    if (res == 0) {
       cfg.gridDim = dim3(static_cast<unsigned>(std::max(2, sms)));
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      if (cudaOccupancyMaxActiveClusters(&res, kern, &cfg) != cudaSuccess || res <= 0) {
         cudaGetLastError();
-        n = std::max(1, sms / 2);
+        res = std::max(1, sms / 2);
       }
-      resident = n;
+      resident.store(res, std::memory_order_relaxed);
     }
-    const int pairs = static_cast<int>(std::min<int64_t>(tiles, std::min(resident, std::max(1, sms / 2))));
+    const int pairs = static_cast<int>(std::min<int64_t>(tiles, std::min(res, std::max(1, sms / 2))));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, td, P);
   } else {
