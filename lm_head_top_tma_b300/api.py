@@ -238,18 +238,39 @@ def profile_read(reset: bool = True) -> dict:
 
 
 class TopKKLLoss(torch.autograd.Function):
-    """Autograd wrapper: loss = kd_topk_kl_forward(H, W, idx, p); the backward
-    calls kd_topk_kl_backward with the incoming gradient as dloss."""
+    """Autograd wrapper of the loss.
+
+    ``mode="separate"`` (default): the forward calls kd_topk_kl_forward and the
+    backward calls kd_topk_kl_backward (recomputing each chunk's logits) with
+    the incoming gradient as dloss.
+    ``mode="fused"`` / ``"fused_norecompute"``: the forward runs the whole fused
+    step (kd_topk_kl_fused_step, or kd_topk_kl_fused_step_norecompute) and keeps
+    dH, dW for dloss = 1; the loss is a scalar and the gradients are linear in
+    dloss, so the backward only scales them.  The kept gradients occupy
+    [T,d] + [V,d] fp32 from forward to backward."""
 
     @staticmethod
-    def forward(ctx, H, W, idx, p, chunk):
-        loss, lse = forward(H, W, idx, p, chunk)
-        ctx.save_for_backward(H, W, idx, p, lse)
-        ctx.chunk = chunk
-        return loss[0]
+    def forward(ctx, H, W, idx, p, chunk, mode="separate"):
+        if mode == "separate":
+            loss, lse = forward(H, W, idx, p, chunk)
+            ctx.save_for_backward(H, W, idx, p, lse)
+            ctx.chunk = chunk
+            ctx.grads = None
+            return loss[0]
+        fn = {"fused": fused_step, "fused_norecompute": fused_step_norecompute}.get(mode)
+        if fn is None:
+            raise ValueError(f"unknown mode {mode!r}")
+        res = fn(H, W, idx, p, chunk)
+        ctx.grads = (res["dH"], res["dW"])
+        ctx.dtypes = (H.dtype, W.dtype)
+        return res["loss"][0]
 
     @staticmethod
     def backward(ctx, g):
+        if ctx.grads is not None:
+            dH, dW = ctx.grads
+            ctx.grads = None
+            return (dH * g).to(ctx.dtypes[0]), (dW * g).to(ctx.dtypes[1]), None, None, None, None
         H, W, idx, p, lse = ctx.saved_tensors
         dH, dW = backward(H, W, idx, p, lse, ctx.chunk, dloss=float(g))
-        return dH.to(H.dtype), dW.to(W.dtype), None, None, None
+        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None

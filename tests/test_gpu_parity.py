@@ -114,12 +114,13 @@ def test_accumulate_and_dloss(tiny):
     assert abs(res["loss"].item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
 
 
-def test_autograd_wrapper(tiny):
+@pytest.mark.parametrize("mode", ["separate", "fused", "fused_norecompute"])
+def test_autograd_wrapper(tiny, mode):
     inp, ref = tiny
     H = inp["H"].clone().requires_grad_(True)
     W = inp["W"].clone().requires_grad_(True)
     idx, p = to_dev(inp["idx"], inp["p"], H.device)
-    loss = api.TopKKLLoss.apply(H, W, idx, p, 64)
+    loss = api.TopKKLLoss.apply(H, W, idx, p, 64, mode)
     (2.0 * loss).backward()
     assert abs(loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
     assert grad_err(H.grad.double().cpu().numpy(), 2.0 * ref["dH"]) <= GRAD_FRAC
