@@ -206,6 +206,15 @@ KD_API kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_
                                      int32_t* idx, float* p, float* lse, void* stream);
 
 /*
+ * dst[i] = bf16(scale * src[i]) (round to nearest even) for i < n: the fp32
+ * gradients dH / dW as bf16 parameter gradients, scaled by an incoming loss
+ * gradient (the paper has no counterpart; a convenience for autograd
+ * wrappers).  src: device fp32, 16-byte aligned; dst: device bf16, 8-byte
+ * aligned; they must not overlap.  Asynchronous on `stream`.
+ */
+KD_API kd_status kd_grad_to_bf16(const float* src, void* dst, int64_t n, float scale, void* stream);
+
+/*
  * Waits for `stream`, then returns and clears the device-side status the
  * last call on this workspace recorded (KD_OK, KD_ERR_BAD_INDEX or
  * KD_ERR_TIMEOUT), or KD_ERR_CUDA if the wait itself failed.

@@ -43,6 +43,7 @@ SIGNATURES = {
     "kd_topk_kl_fused_step_norecompute": (_i32, [_c_p, _c_p, _c_p, _c_p, _i64, _i32, _i32, _i32, _i32,
                                                  _f32, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _c_p, _sz, _c_p]),
     "kd_topk_cache_build": (_i32, [_c_p, _i32, _i64, _i32, _i32, _c_p, _c_p, _c_p, _c_p]),
+    "kd_grad_to_bf16": (_i32, [_c_p, _c_p, _i64, _f32, _c_p]),
     "kd_topk_kl_device_status": (_i32, [_c_p, _c_p]),
     "kd_topk_kl_forward_noalloc": (_i32, [_c_p, _c_p, _c_p, _c_p, _i64, _i32, _i32, _i32, _i32,
                                           _c_p, _c_p, _c_p, _c_p]),

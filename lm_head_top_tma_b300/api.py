@@ -13,7 +13,7 @@ import torch
 from . import _native as N
 
 __all__ = ["workspace_size", "Workspace", "forward", "forward_noalloc", "backward", "fused_step",
-           "fused_step_norecompute", "topk_cache_build",
+           "fused_step_norecompute", "topk_cache_build", "grad_to_bf16",
            "device_status", "gemm_bf16", "debug_wait_timeout", "TopKKLLoss",
            "profile_enable", "profile_read"]
 
@@ -205,6 +205,15 @@ def topk_cache_build(Z, K: int, *, lse: bool = True):
     return idx, p, l
 
 
+def grad_to_bf16(g: torch.Tensor, scale: float = 1.0) -> torch.Tensor:
+    """bf16(scale * g) for an fp32 CUDA gradient (kd_grad_to_bf16)."""
+    _need(g, "g", torch.float32, g.dim())
+    out = torch.empty(g.shape, dtype=torch.bfloat16, device=g.device)
+    N.check(N.load().kd_grad_to_bf16(_ptr(g), _ptr(out), g.numel(), float(scale), _stream(g.device)),
+            "kd_grad_to_bf16")
+    return out
+
+
 def gemm_bf16(A, B, M, N_, K, *, a_mn=False, b_mn=False, cta_pair=False, out=None, check=True):
     """D = A B^T on the library's tcgen05 GEMM (A [M,K] or [K,M]; B [N,K] or [K,N]);
     ``cta_pair`` selects the two-CTA-cluster form."""
@@ -262,7 +271,6 @@ class TopKKLLoss(torch.autograd.Function):
             raise ValueError(f"unknown mode {mode!r}")
         res = fn(H, W, idx, p, chunk)
         ctx.grads = (res["dH"], res["dW"])
-        ctx.dtypes = (H.dtype, W.dtype)
         return res["loss"][0]
 
     @staticmethod
@@ -270,7 +278,10 @@ class TopKKLLoss(torch.autograd.Function):
         if ctx.grads is not None:
             dH, dW = ctx.grads
             ctx.grads = None
-            return (dH * g).to(ctx.dtypes[0]), (dW * g).to(ctx.dtypes[1]), None, None, None, None
-        H, W, idx, p, lse = ctx.saved_tensors
-        dH, dW = backward(H, W, idx, p, lse, ctx.chunk, dloss=float(g))
-        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None
+            scale = float(g)
+        else:
+            H, W, idx, p, lse = ctx.saved_tensors
+            dH, dW = backward(H, W, idx, p, lse, ctx.chunk, dloss=float(g))
+            scale = 1.0
+        # H and W are bf16 (the C ABI's input type): their gradients are too
+        return grad_to_bf16(dH, scale), grad_to_bf16(dW, scale), None, None, None, None

@@ -198,6 +198,26 @@ __global__ void kd_dh_reduce_kernel(const float4* __restrict__ part, int S, int6
   }
 }
 
+// dst[i] = bf16(scale * src[i]) (round to nearest even), 4 elements per thread
+// when both pointers allow 16-/8-byte accesses.
+__global__ void kd_scale_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t n,
+                                        float scale) {
+  const int64_t n4 = n / 4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(src)[i];
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&a);
+    w.y = *reinterpret_cast<uint32_t*>(&b);
+    reinterpret_cast<uint2*>(dst)[i] = w;
+  }
+  for (int64_t i = n4 * 4 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = __float2bfloat16_rn(src[i] * scale);
+}
+
 constexpr int GPASS_THREADS = 256;
 constexpr int GPASS_VEC = 8;     // bf16 per 16-byte access
 constexpr int GPASS_UNROLL = 4;  // accesses in flight per thread

@@ -621,6 +621,18 @@ kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, in
   return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
+kd_status kd_grad_to_bf16(const float* src, void* dst, int64_t n, float scale, void* stream) {
+  if (!src || !dst || n < 0) return KD_ERR_INVALID_ARG;
+  if (n == 0) return KD_OK;
+  if (!aligned16(src) || (reinterpret_cast<uintptr_t>(dst) & 7u)) return KD_ERR_UNSUPPORTED;
+  if (!device_supported()) return KD_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t blocks = std::min<int64_t>(std::max<int64_t>(1, ceil_div(n / 4, 256)), 8L * current_sm_count());
+  kd_scale_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, static_cast<__nv_bfloat16*>(dst), n,
+                                                                         scale);
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
 kd_status kd_topk_kl_device_status(void* workspace, void* stream) {
   if (!workspace) return KD_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -135,3 +135,14 @@ def test_gradient_rows_sum_to_zero_on_gpu(tiny):
     col = np.abs(got["dW"].sum(axis=0)).max()
     bound = inp["H"].shape[0] * 2 * 2.0 ** -9 * inp["H"].float().abs().max().item()
     assert col <= bound
+
+
+@pytest.mark.parametrize("n", [1, 7, 4096, 1000003])
+def test_grad_to_bf16_rounds_like_torch(cuda_device, n):
+    """kd_grad_to_bf16: bf16(scale * x), round to nearest even, any length."""
+    g = torch.Generator(device=cuda_device).manual_seed(n)
+    x = torch.randn(n, generator=g, device=cuda_device) * 3.0
+    got = api.grad_to_bf16(x, -0.37)
+    ref = (x * -0.37).to(torch.bfloat16)   # fp32 product rounded once to bf16, the same two steps
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
