@@ -58,6 +58,11 @@ def test_tiny_forward_then_backward(tiny):
     (513, 64, 300, 9, 513),        # 3 pair tiles, one ragged row; the peer's half of the
                                    # second vocabulary tile lies wholly past V
     (1100, 136, 1030, 32, 1024),   # two chunks of a pair-tiled size, dW grouped over both
+    # degenerate and extreme sizes:
+    (40, 64, 4096, 1024, 32),      # K at its maximum
+    (700, 8, 2000, 10, 512),       # d at its minimum (one 16-byte row), pair tiles
+    (50, 64, 1, 1, 16),            # a one-word vocabulary: softmax is 1, G = M - p
+    (9, 32, 300, 3, 1),            # one row per chunk
 ])
 def test_edge_shapes(cuda_device, T, d, V, K, chunk):
     H, W = make_hw(T, d, V, "uniform", seed=T + V, device=cuda_device)
