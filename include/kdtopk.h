@@ -45,6 +45,11 @@
  *   - Concurrency: calls that share a workspace must be ordered on one
  *     stream.  Apart from the optional profiler (kd_profile_*), the library
  *     keeps no mutable global state.
+ *   - CUDA graphs: forward, backward and both fused steps only launch kernels
+ *     and set the workspace's status word on `stream`, so they can be
+ *     captured and replayed (inputs, outputs and workspace at fixed
+ *     addresses); read the status with kd_topk_kl_device_status outside the
+ *     captured region.
  */
 #ifndef KDTOPK_H
 #define KDTOPK_H
