@@ -21,57 +21,110 @@ namespace kd {
 
 constexpr int PREP_WARPS = 4;
 
-// One warp per chunk row; a bitonic network over Kpad (power of two >= K)
-// slots in shared memory, padded with INT_MAX ids.
+// One warp per chunk row.  The row's K (id, p) pairs are held in registers,
+// EPT = Kpad / 32 consecutive slots per lane (Kpad: the power of two >= K,
+// padding ids INT_MAX), loaded 16 bytes at a time when the row allows it, and
+// sorted ascending by id with a bitonic network: exchanges across lanes by
+// shuffles, within a lane by register swaps.  Equal ids keep their pairs
+// (neither partner takes the other's), so duplicates survive intact.
+template <int EPT>
 __global__ void __launch_bounds__(PREP_WARPS * 32)
     kd_prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ p, int rows_valid,
-                   int Cpad, int K, int Kpad, int V, int32_t* __restrict__ sidx, float* __restrict__ sp,
+                   int Cpad, int K, int V, int vec_rows, int32_t* __restrict__ sidx, float* __restrict__ sp,
                    float* __restrict__ rowM, float* __restrict__ rowE, int* status) {
-  extern __shared__ uint8_t sm_raw[];
+  constexpr int N = 32 * EPT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * PREP_WARPS + warp;
   if (r >= Cpad) return;
-  int32_t* key = reinterpret_cast<int32_t*>(sm_raw) + warp * 2 * Kpad;
-  float* val = reinterpret_cast<float*>(key + Kpad);
   const bool live = r < rows_valid;
-  bool bad = false;
-  for (int k = lane; k < Kpad; k += 32) {
-    int id = INT_MAX;
-    float pv = 0.f;
-    if (live && k < K) {
-      id = __ldg(idx + static_cast<size_t>(r) * K + k);
-      pv = __ldg(p + static_cast<size_t>(r) * K + k);
-      if (id < 0 || id >= V) bad = true;
-    }
-    key[k] = id;
-    val[k] = pv;
+  const int e0 = lane * EPT;  // this lane's first slot
+  int key[EPT];
+  float val[EPT];
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    key[i] = INT_MAX;
+    val[i] = 0.f;
   }
-  bad = __any_sync(0xffffffffu, bad);
-  __syncwarp();
-  for (int size = 2; size <= Kpad; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = lane; i < Kpad; i += 32) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool up = (i & size) == 0;
-          const int a = key[i], b = key[j];
-          if ((a > b) == up) {
-            key[i] = b;
-            key[j] = a;
-            const float t = val[i];
-            val[i] = val[j];
-            val[j] = t;
+  bool bad = false;
+  if (live) {
+    const int32_t* ir = idx + static_cast<size_t>(r) * K;
+    const float* pr = p + static_cast<size_t>(r) * K;
+    if constexpr (EPT >= 4) {
+      if (vec_rows) {  // K % 4 == 0 and 16-byte aligned rows
+#pragma unroll
+        for (int i = 0; i < EPT; i += 4) {
+          if (e0 + i < K) {  // K % 4 == 0: the whole 4-slot group is valid
+            const int4 a = __ldg(reinterpret_cast<const int4*>(ir + e0 + i));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(pr + e0 + i));
+            key[i] = a.x;
+            key[i + 1] = a.y;
+            key[i + 2] = a.z;
+            key[i + 3] = a.w;
+            val[i] = b.x;
+            val[i + 1] = b.y;
+            val[i + 2] = b.z;
+            val[i + 3] = b.w;
           }
         }
       }
-      __syncwarp();
+    }
+    if (!(EPT >= 4 && vec_rows)) {
+#pragma unroll
+      for (int i = 0; i < EPT; ++i)
+        if (e0 + i < K) {
+          key[i] = __ldg(ir + e0 + i);
+          val[i] = __ldg(pr + e0 + i);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < EPT; ++i)
+      if (e0 + i < K && (key[i] < 0 || key[i] >= V)) bad = true;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= EPT) {  // partner slot in lane ^ (stride / EPT), same position
+        const int lm = stride / EPT;
+        const bool lower = (lane & lm) == 0;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+          const bool up = ((e0 + i) & size) == 0;
+          const int k2 = __shfl_xor_sync(0xffffffffu, key[i], lm);
+          const float v2 = __shfl_xor_sync(0xffffffffu, val[i], lm);
+          const bool take = (lower == up) ? (k2 < key[i]) : (k2 > key[i]);
+          if (take) {
+            key[i] = k2;
+            val[i] = v2;
+          }
+        }
+      } else {  // both slots in this lane
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+          if ((i & stride) == 0) {
+            const int j = i | stride;
+            const bool up = ((e0 + i) & size) == 0;
+            if ((key[i] > key[j]) == up) {
+              const int tk = key[i];
+              key[i] = key[j];
+              key[j] = tk;
+              const float tv = val[i];
+              val[i] = val[j];
+              val[j] = tv;
+            }
+          }
+        }
+      }
     }
   }
+
   float m = 0.f, e = 0.f;
-  for (int k = lane; k < K; k += 32) {
-    const float pv = val[k];
-    m += pv;
-    if (pv > 0.f) e += pv * logf(pv);
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    m += val[i];
+    if (val[i] > 0.f) e += val[i] * logf(val[i]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -81,10 +134,32 @@ __global__ void __launch_bounds__(PREP_WARPS * 32)
   if (bad) {  // the row contributes nothing; the caller learns it from the status word
     m = 0.f;
     e = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+      key[i] = INT_MAX;
+      val[i] = 0.f;
+    }
   }
-  for (int k = lane; k < K; k += 32) {
-    sidx[static_cast<size_t>(r) * K + k] = bad ? INT_MAX : key[k];
-    sp[static_cast<size_t>(r) * K + k] = bad ? 0.f : val[k];
+  int32_t* so = sidx + static_cast<size_t>(r) * K;
+  float* po = sp + static_cast<size_t>(r) * K;
+  if constexpr (EPT >= 4) {
+    if (vec_rows) {
+#pragma unroll
+      for (int i = 0; i < EPT; i += 4) {
+        if (e0 + i < K) {
+          *reinterpret_cast<int4*>(so + e0 + i) = make_int4(key[i], key[i + 1], key[i + 2], key[i + 3]);
+          *reinterpret_cast<float4*>(po + e0 + i) = make_float4(val[i], val[i + 1], val[i + 2], val[i + 3]);
+        }
+      }
+    }
+  }
+  if (!(EPT >= 4 && vec_rows)) {
+#pragma unroll
+    for (int i = 0; i < EPT; ++i)
+      if (e0 + i < K) {
+        so[e0 + i] = key[i];
+        po[e0 + i] = val[i];
+      }
   }
   if (lane == 0) {
     rowM[r] = m;

@@ -383,11 +383,8 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
 
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
 
-  const size_t prep_smem = size_t(PREP_WARPS) * pl.Kpad * 8;
-  if (prep_smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(prep_smem)) != cudaSuccess)
-    return KD_ERR_CUDA;
+  // rows of the id / probability cache that 16-byte loads can read
+  const int vec_rows = (K % 4 == 0 && aligned16(idx) && aligned16(p)) ? 1 : 0;
 
   const bool keep = (mode & MODE_KEEP) != 0;
   const int kb_d = static_cast<int>(ceil_div(d, BK));
@@ -425,9 +422,21 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   // ---- the steps of one chunk
   auto prep = [&](int c) {
     const int slot = prof_begin(KD_K_PREP, st);
-    kd_prep_kernel<<<static_cast<unsigned>(ceil_div(pl.Cpad, PREP_WARPS)), PREP_WARPS * 32, prep_smem, st>>>(
-        idx + t0_of(c) * K, p + t0_of(c) * K, rows_of(c), pl.Cpad, K, pl.Kpad, V, sidx_of(c), sp_of(c), rowM_of(c),
-        rowE_of(c), status);
+    const unsigned blocks = static_cast<unsigned>(ceil_div(pl.Cpad, PREP_WARPS));
+    const int32_t* ic = idx + t0_of(c) * K;
+    const float* pc = p + t0_of(c) * K;
+#define KD_PREP(EPT)                                                                                          \
+  kd_prep_kernel<EPT><<<blocks, PREP_WARPS * 32, 0, st>>>(ic, pc, rows_of(c), pl.Cpad, K, V, vec_rows, sidx_of(c), \
+                                                         sp_of(c), rowM_of(c), rowE_of(c), status)
+    switch (pl.Kpad) {
+      case 32: KD_PREP(1); break;
+      case 64: KD_PREP(2); break;
+      case 128: KD_PREP(4); break;
+      case 256: KD_PREP(8); break;
+      case 512: KD_PREP(16); break;
+      default: KD_PREP(32); break;  // Kpad 1024 (K <= 1024 is checked)
+    }
+#undef KD_PREP
     const cudaError_t e = cudaGetLastError();
     prof_end(slot, st);
     return check(e);
