@@ -4,19 +4,25 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload longctx]
     python bench.py --impl reference ...      # the fp64 CPU oracle, timed on host cores
 
+    python bench.py --sweep                   # output-head-only T sweep, one line per T
+    python bench.py --topk-cache              # the teacher-cache builder
+
 One step = one ``kd_topk_kl_fused_step`` over the whole workload: every chunk's
 prep, logits GEMM with fused softmax partials and top-K gather, combine,
-logits GEMM again with the gradient epilogue, dH = G W and dW += G^T H.
-Default workload: the long-context head (T 32768, d 3072, V 128256, K 100,
-chunk 2048).  Inputs are seeded synthetic tensors of that shape; W alone
-(788 MB) is larger than L2, so no flush is needed between steps.
+logits GEMM again with the gradient epilogue (merged with the next chunk's
+forward GEMM), dH = G W and dW += G^T H.  Default workload: the long-context
+head (T 32768, d 3072, V 128256, K 100, chunk 2048).  Inputs are seeded
+synthetic tensors of that shape; W alone (788 MB) is larger than L2, so no
+flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  ``value`` is tokens/s of the whole job with
 inputs resident in HBM; ``e2e`` repeats the measurement through the public
-API with the step's inputs (H, idx, p) copied from pinned host memory and the
-loss read back every step.  N > 1 runs one independent replica per GPU
-(torchrun; the path needs no data exchange for this metric), timed between
-barriers, max over ranks.
+API with the step's inputs (H, idx, p) copied from pinned host memory (on a
+side stream, one step ahead, into two device buffers) and the loss read back
+every step; ``variants.fused_norecompute`` times the fused step without the
+backward recompute in the same run.  N > 1 runs one independent replica per
+GPU (torchrun; the path needs no data exchange for this metric), timed
+between barriers, max over ranks.
 """
 from __future__ import annotations
 
