@@ -47,9 +47,10 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 # of two 2048-row chunks, the first group of a step stores dW ("first"), the
 # others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
 # chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": "3b5c948abd4840a7", "kinds": {
-    "gemm_dw": {"first": 1452616704 + 1545390336, "rest": 2782197760 + 1538707200},
-    "logits_gf": {"first": 893756416 + 523619840, "rest": 893756416 + 523619840},
+TRAFFIC = {"workload": "longctx", "src_sha": "d102f076905a1606", "kinds": {
+    "gemm_dw": {"first": 1362949888 + 1544164096, "rest": 2755587584 + 1536736512},
+    "logits_gf": {"first": 1126369536 + 522738432,
+                  "rest": (864735744 + 522315776 + 911572224 + 522344192) // 2},
 }}
 KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300/csrc/kd_ptx.cuh",
                   "lm_head_top_tma_b300/csrc/kdtopk.cu"]
