@@ -47,7 +47,7 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 # of two 2048-row chunks, the first group of a step stores dW ("first"), the
 # others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
 # chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": "d102f076905a1606", "kinds": {
+TRAFFIC = {"workload": "longctx", "src_sha": "fae53b511ca64e08", "kinds": {
     "gemm_dw": {"first": 1362949888 + 1544164096, "rest": 2755587584 + 1536736512},
     "logits_gf": {"first": 1126369536 + 522738432,
                   "rest": (864735744 + 522315776 + 911572224 + 522344192) // 2},
@@ -56,11 +56,25 @@ KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300
                   "lm_head_top_tma_b300/csrc/kdtopk.cu"]
 
 
-def kernel_src_sha() -> str:
+def _code_only(src: str) -> str:
+    """C/C++ source without comments and whitespace: what the compiler sees."""
+    import re
+
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return re.sub(r"\s+", "", src)
+
+
+def kernel_src_sha(read=None) -> str:
+    """Hash of the kernel sources' code (comments and layout excluded)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(ROOT, f)) as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(_code_only(text).encode())
     return h.hexdigest()[:16]
 
 

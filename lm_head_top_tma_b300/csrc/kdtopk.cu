@@ -12,9 +12,13 @@
 //   backward  logits GEMM again with G = M softmax - p formed in the epilogue
 //             (bf16 [chunk, V] operand), dH = G W (split-K, then a reduction),
 //             dW += G^T H (fp32 read-modify-write of the caller's dW)
-// The no-recompute fused step keeps the forward's tile-normalised exponentials
-// in the G buffer and forms G from them elementwise once lse is known, so the
-// backward starts at dH.
+// The fused step is pipelined by one chunk: chunk c's G GEMM and chunk c+1's
+// forward GEMM run as one launch over both chunks' rows (they share every W
+// tile).  The no-recompute fused step keeps the forward's tile-normalised
+// exponentials in the G buffer and forms G from them elementwise once lse is
+// known, so the backward starts at dH.  The teacher-cache builder (top-K ids
+// and probabilities of teacher logits) and a gradient scale-and-round helper
+// complete the ABI.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
