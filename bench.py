@@ -96,7 +96,17 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+        # nvidia-smi numbers GPUs physically; CUDA may renumber them (CUDA_VISIBLE_DEVICES),
+        # so the sampled GPU is named by its UUID when torch reports one
+        self.gpu = str(gpu_index)
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            if uuid:
+                self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
         self.proc = None
         self.path = None
 
