@@ -323,6 +323,7 @@ def run_kdtopk(args):
     ms = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms, ws)
     tokens_per_s = ws * T / (ms / 1e3)
+    peak_bytes = torch.cuda.max_memory_allocated(dev)  # inputs + outputs + workspace of the step
 
     # ---- end to end: every step's inputs copied in from pinned host memory and its loss
     # read back.  The copies run on a side stream into two device buffers, so step k+1's
@@ -374,7 +375,6 @@ def run_kdtopk(args):
     barrier(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws)
     h2d = Hh.numel() * Hh.element_size() + ih.numel() * 4 + ph.numel() * 4
-    peak_bytes = torch.cuda.max_memory_allocated(dev)
     launches = sum(n for _, n in prof.values()) + prof["combine"][1]  # the loss reduction rides with combine
 
     # ---- the same step without the backward recompute (kept exponentials -> G)
