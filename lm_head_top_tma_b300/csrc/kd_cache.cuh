@@ -6,24 +6,31 @@
 // aimodeling.com "First cut": top-100 probabilities cached for every token),
 // here over logits that are already on the device.
 //
-// One block of 512 threads per row (grid-stride over rows, several blocks per
-// SM); the row is read from HBM once (16-byte loads, several in flight per
-// thread) and a second time from L2:
-//   pass 1  per-slot maximum key (1024 slots: two per thread, every element in
-//           exactly one) and an online (max, sum of 2^x) for lse;
+// One block of 512 threads per row (grid-stride over rows, two blocks per
+// SM); each row is read from HBM once, with 16-byte loads, several in flight
+// per thread, after an L2 prefetch of the whole row:
+//   pass 1  per-slot maximum (1024 slots: two per thread, every element in
+//           exactly one), an online (max, sum of 2^x) for lse, and the maximum
+//           of every 16-byte group, kept in shared memory (as bf16, rounded up
+//           for fp32 logits);
 //   select  theta = the K-th largest slot maximum, by a binary search over the
 //           key space with block-wide counts: at least K distinct elements
 //           reach theta, so every top-K element has key >= theta;
-//   pass 2  collect the elements with key >= theta (typically a few hundred)
-//           into shared memory; rank them by (key descending, id ascending)
-//           by counting (bitonic sort above 1024 candidates);
-//   fallback  when more than CACHE_CAP elements reach theta (heavily tied or
+//   pass 2  only the groups whose maximum reaches theta (typically about K of
+//           them) are read again, from L2, and their elements >= theta are
+//           collected in shared memory; they are ranked by (key descending,
+//           id ascending) by counting (bitonic sort above 1024 candidates);
+//   fallback  rows whose group maxima do not fit in shared memory, or that
+//           cannot be read 16 bytes at a time, are scanned whole in pass 2;
+//           when more than CACHE_CAP elements reach theta (heavily tied or
 //           adversarial rows) the exact K-th key is found by a binary search
 //           over the key space, and the tied elements at it are taken in
 //           ascending id order by an ordered block scan.
 // Keys are the order-preserving unsigned images of the logits (sign bit
 // flipped for positives, all bits for negatives, -0 folded onto +0), so
-// comparisons are exact and equal logits have equal keys.
+// comparisons are exact and equal logits have equal keys.  A candidate is the
+// composite (~key << 32 | id): ascending composites are the output order, and
+// the logit is recovered from the key, so p needs no second read of Z.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -41,6 +48,12 @@ constexpr int CACHE_THREADS = 512;
 constexpr int CACHE_SLOTS = 2 * CACHE_THREADS;  // per-row maxima used to bound the K-th key
 constexpr int CACHE_CAP = 4096;                 // candidates kept in shared memory
 constexpr int CACHE_UNROLL = 4;                 // 16-byte loads in flight per thread
+constexpr int CACHE_GMAX = 32768;               // 16-byte group maxima kept in shared memory
+constexpr int CACHE_GLIST = 1024;               // groups listed for the re-read of pass 2
+
+// dynamic shared memory of kd_topk_cache_kernel: the candidate list, and the
+// group maxima when rows are read 16 bytes at a time
+constexpr int cache_smem_bytes(bool vec) { return CACHE_CAP * 8 + (vec ? CACHE_GMAX * 2 : 0); }
 
 template <typename T>
 struct LogitTraits;
@@ -139,20 +152,8 @@ __device__ __forceinline__ int block_sum_int(int v, int* red) {
   return t;
 }
 
-// Online softmax normaliser over logits x (natural units): (m, s) with
-// m the running maximum and s = sum 2^((x - m) log2 e); -inf logits add nothing.
-template <int N>
-__device__ __forceinline__ void lse_fold(float& m, float& s, float xmax, const float (&x)[N]) {
-  if (xmax == -INFINITY) return;
-  if (xmax > m) {
-    s *= ex2((m - xmax) * kLog2e);
-    m = xmax;
-  }
-  const float nm = -m * kLog2e;
-#pragma unroll
-  for (int i = 0; i < N; ++i) s += ex2(fmaf(x[i], kLog2e, nm));
-}
-
+// Merges two online softmax normalisers (m, s) over logits in natural units:
+// s = sum 2^((x - m) log2 e) over the logits seen, m their running maximum.
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
   const float mn = fmaxf(m, m2);
   s = (mn == -INFINITY) ? 0.f : s * ex2((m - mn) * kLog2e) + s2 * ex2((m2 - mn) * kLog2e);
@@ -180,7 +181,117 @@ struct RowView {
     if constexpr (VEC) LogitTraits<TL>::unpack(r, f);
     else f[0] = LogitTraits<TL>::value(r);
   }
+  // the largest value of a loaded group
+  __device__ static float gmax(const Raw& r) {
+    if constexpr (VEC) return LogitTraits<TL>::group_max(r);
+    else return LogitTraits<TL>::value(r);
+  }
 };
+
+// Appends the candidate (key, id) to the block's list; entries past
+// CACHE_CAP are counted but not stored.
+__device__ __forceinline__ void push_cand(uint64_t* cand, int* count, uint32_t key, int id) {
+  const int at = atomicAdd(count, 1);
+  if (at < CACHE_CAP) cand[at] = (static_cast<uint64_t>(~key) << 32) | static_cast<uint32_t>(id);
+}
+
+// One byte-level step of a most-significant-byte-first radix select of the
+// K-th largest of the block's 2 * CACHE_THREADS keys (two per thread), after
+// every thread has counted its keys that share `prefix` into hist[256] by the
+// byte at `shift` and the block has synchronised.  Warp 0 picks the byte b of
+// the K-th largest, stores (b, keys above b's bin) in sel[0..1] and clears
+// hist for its next use; the caller synchronises before reading sel.
+__device__ __forceinline__ void radix_pick(int* hist, int* sel, int need) {
+  const int lane = threadIdx.x & 31;
+  int h[8];
+  int sum = 0;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    h[b] = hist[lane * 8 + b];
+    hist[lane * 8 + b] = 0;
+    sum += h[b];
+  }
+  int incl = sum;  // keys in the bins of lanes >= lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += v;
+  }
+  const int above = incl - sum;  // keys in the bins of lanes > lane
+  if (above < need && incl >= need) {
+    int acc = above;
+#pragma unroll
+    for (int b = 7; b >= 0; --b) {
+      if (acc + h[b] >= need) {
+        sel[0] = lane * 8 + b;
+        sel[1] = acc;
+        break;
+      }
+      acc += h[b];
+    }
+  }
+}
+
+// Counts key k into hist by its byte at `shift` when its bytes above `shift`
+// equal `prefix`.
+template <int KEY_BITS>
+__device__ __forceinline__ void radix_count(uint32_t k, int shift, uint32_t prefix, int* hist) {
+  const int hs = shift + 8;
+  if (hs >= KEY_BITS || (k >> hs) == prefix) atomicAdd(&hist[(k >> shift) & 255], 1);
+}
+
+// bf16 bits of a group maximum, never below it: exact for bf16 logits,
+// rounded up for fp32 ones (a group is re-read when this reaches theta).
+template <typename TL>
+__device__ __forceinline__ uint16_t gmax_bits(float x) {
+  if constexpr (std::is_same<TL, __nv_bfloat16>::value) return static_cast<uint16_t>(__float_as_uint(x) >> 16);
+  else return __bfloat16_as_ushort(__float2bfloat16_ru(x));
+}
+
+// Statistics of U loaded groups x[0..U): the slot maximum, the online
+// normaliser (m, s), folded group after group, and each group's maximum in
+// gm[u].
+template <int U, typename RV>
+__device__ __forceinline__ void groups_stats(const typename RV::Raw (&x)[U], float (&gm)[U], float& m, float& s,
+                                             float& slot) {
+  constexpr int PV = RV::PV;
+  float fmx = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    gm[u] = RV::gmax(x[u]);
+    fmx = fmaxf(fmx, gm[u]);
+  }
+  slot = fmaxf(slot, fmx);
+  if (fmx == -INFINITY) return;  // -inf logits add nothing
+  if (fmx > m) {
+    s *= ex2((m - fmx) * kLog2e);
+    m = fmx;
+  }
+  const float nm = -m * kLog2e;
+  if constexpr (PV == 1) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float f[1];
+      RV::floats(x[u], f);
+      s += ex2(fmaf(f[0], kLog2e, nm));
+    }
+  } else {
+    // two logits per packed fp32 FMA / add (Blackwell f32x2)
+    const float2 l2 = make_float2(kLog2e, kLog2e), nm2 = make_float2(nm, nm);
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float f[PV];
+      RV::floats(x[u], f);
+#pragma unroll
+      for (int i = 0; i < PV; i += 2) {
+        const float2 t = __ffma2_rn(make_float2(f[i], f[i + 1]), l2, nm2);
+        acc = __fadd2_rn(acc, make_float2(ex2(t.x), ex2(t.y)));
+      }
+    }
+    s += acc.x + acc.y;
+  }
+}
 
 template <typename TL, bool VEC>
 __global__ void __launch_bounds__(CACHE_THREADS, 2)
@@ -189,124 +300,167 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
   using Tr = LogitTraits<TL>;
   using RV = RowView<TL, VEC>;
   constexpr int PV = RV::PV;
-  __shared__ uint64_t cand[CACHE_CAP];  // (~key << 32) | id: ascending = key descending, id ascending
+  constexpr int NW = CACHE_THREADS / 32;
+  extern __shared__ __align__(16) unsigned char cache_smem[];
+  uint64_t* cand = reinterpret_cast<uint64_t*>(cache_smem);  // (~key << 32) | id
+  uint16_t* gmax = reinterpret_cast<uint16_t*>(cache_smem + CACHE_CAP * 8);  // used when VEC
   __shared__ float red_m[32], red_s[32];
   __shared__ int red_i[32];
-  __shared__ int s_count;
+  __shared__ int hist[256];  // radix-select counts, zero between uses
+  __shared__ int sel[2];
+  __shared__ int glist[CACHE_GLIST];  // groups re-read in pass 2
+  __shared__ int s_count, s_groups;
   __shared__ float s_lse;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  constexpr int NW = CACHE_THREADS / 32;
+  for (int i = tid; i < 256; i += CACHE_THREADS) hist[i] = 0;
 
   for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
     const RV rv{Z + row * static_cast<int64_t>(V), V};
     const int ng = rv.groups();
-    // ---------------- pass 1: slot maxima, online softmax normaliser
+    const bool screen = VEC && ng <= CACHE_GMAX;  // group maxima fit in shared memory
+    if constexpr (VEC) {
+      if (tid == 0) prefetch_l2_bulk(rv.z, static_cast<int64_t>(V) * sizeof(TL));
+    }
+    // ---------------- pass 1: slot maxima, online softmax normaliser, group maxima
     float fslot0 = -INFINITY, fslot1 = -INFINITY;  // two disjoint element sets per thread
     float m = -INFINITY, s = 0.f;
-    int it = 0;
+    int it = 0;  // the slot of an iteration alternates
     for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL, ++it) {
+      float& slot = (it & 1) ? fslot1 : fslot0;
       if (g0 + (CACHE_UNROLL - 1) * CACHE_THREADS < ng) {
-        // all groups present: one rescale check for CACHE_UNROLL * PV logits
         typename RV::Raw x[CACHE_UNROLL];
+        float gm[CACHE_UNROLL];
 #pragma unroll
         for (int u = 0; u < CACHE_UNROLL; ++u) x[u] = rv.load(g0 + u * CACHE_THREADS);
-        float f[CACHE_UNROLL * PV];
+        groups_stats<CACHE_UNROLL, RV>(x, gm, m, s, slot);
+        if (screen) {
 #pragma unroll
-        for (int u = 0; u < CACHE_UNROLL; ++u) {
-          float fu[PV];
-          RV::floats(x[u], fu);
-#pragma unroll
-          for (int i = 0; i < PV; ++i) f[u * PV + i] = fu[i];
+          for (int u = 0; u < CACHE_UNROLL; ++u) gmax[g0 + u * CACHE_THREADS] = gmax_bits<TL>(gm[u]);
         }
-        float fmx = f[0];
-#pragma unroll
-        for (int i = 1; i < CACHE_UNROLL * PV; ++i) fmx = fmaxf(fmx, f[i]);
-        lse_fold(m, s, fmx, f);
-        if (it & 1) fslot1 = fmaxf(fslot1, fmx);
-        else fslot0 = fmaxf(fslot0, fmx);
       } else {
         for (int u = 0; u < CACHE_UNROLL && g0 + u * CACHE_THREADS < ng; ++u) {
-          float f[PV];
-          RV::floats(rv.load(g0 + u * CACHE_THREADS), f);
-          float fmx = f[0];
-#pragma unroll
-          for (int i = 1; i < PV; ++i) fmx = fmaxf(fmx, f[i]);
-          lse_fold(m, s, fmx, f);
-          if (it & 1) fslot1 = fmaxf(fslot1, fmx);
-          else fslot0 = fmaxf(fslot0, fmx);
+          const typename RV::Raw x[1] = {rv.load(g0 + u * CACHE_THREADS)};
+          float gm[1];
+          groups_stats<1, RV>(x, gm, m, s, slot);
+          if (screen) gmax[g0 + u * CACHE_THREADS] = gmax_bits<TL>(gm[0]);
         }
       }
     }
     if constexpr (VEC) {  // the tail that does not fill a 16-byte vector
       for (int j = ng * PV + tid; j < V; j += CACHE_THREADS) {
-        const float f[1] = {Tr::value(rv.z[j])};
-        lse_fold(m, s, f[0], f);
-        fslot1 = fmaxf(fslot1, f[0]);
+        const TL x[1] = {rv.z[j]};
+        float gm[1];
+        groups_stats<1, RowView<TL, false>>(x, gm, m, s, fslot1);
       }
     }
     // slots without elements hold -inf: no larger than any element, so they never raise theta
     const uint32_t kslot0 = Tr::fkey(fslot0), kslot1 = Tr::fkey(fslot1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
-    __syncthreads();  // the previous row's shared state is no longer read
+    __syncthreads();  // the previous row's shared state is no longer read (and hist is clear)
+    // ---------------- theta: the K-th largest of the 1024 slot maxima, by radix
+    // select one byte at a time; the block's lse is reduced alongside
     if (lane == 0) {
       red_m[warp] = m;
       red_s[warp] = s;
     }
-    if (tid == 0) s_count = 0;
-    __syncthreads();
-    if (warp == 0) {
-      float mm = lane < NW ? red_m[lane] : -INFINITY;
-      float ss = lane < NW ? red_s[lane] : 0.f;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lse_merge(mm, ss, __shfl_xor_sync(0xffffffffu, mm, o), __shfl_xor_sync(0xffffffffu, ss, o));
-      if (lane == 0) s_lse = mm + log2f(ss) * kLn2;
+    if (tid == 0) {
+      s_count = 0;
+      s_groups = 0;
     }
-    // ---------------- theta: the K-th largest of the 1024 slot maxima (slots
-    // without elements hold key 0, the smallest key)
-    uint64_t lo = 0, hi = (Tr::KEY_BITS == 32) ? 0xFFFFFFFFull : 0xFFFFull;
-    while (lo < hi) {
-      const uint64_t mid = lo + (hi - lo + 1) / 2;
-      const int c = __syncthreads_count(kslot0 >= mid) + __syncthreads_count(kslot1 >= mid);
-      if (c >= K) lo = mid;
-      else hi = mid - 1;
-    }
-    const uint32_t theta = static_cast<uint32_t>(lo);
-
-    // ---------------- pass 2: candidates with key >= theta, i.e. value >= theta's value
-    const float tv = Tr::kvalue(theta);
-    for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL) {
-      typename RV::Raw x[CACHE_UNROLL];
+    uint32_t prefix = 0;  // the bytes of theta found so far
+    int need = K;         // theta's rank among the keys that share them
 #pragma unroll
-      for (int u = 0; u < CACHE_UNROLL; ++u)
-        if (g0 + u * CACHE_THREADS < ng) x[u] = rv.load(g0 + u * CACHE_THREADS);
+    for (int shift = Tr::KEY_BITS - 8; shift >= 0; shift -= 8) {
+      radix_count<Tr::KEY_BITS>(kslot0, shift, prefix, hist);
+      radix_count<Tr::KEY_BITS>(kslot1, shift, prefix, hist);
+      __syncthreads();
+      if (warp == 0) {
+        radix_pick(hist, sel, need);
+        if (shift == Tr::KEY_BITS - 8) {
+          float mm = lane < NW ? red_m[lane] : -INFINITY;
+          float ss = lane < NW ? red_s[lane] : 0.f;
 #pragma unroll
-      for (int u = 0; u < CACHE_UNROLL; ++u) {
-        const int g = g0 + u * CACHE_THREADS;
-        if (g >= ng) break;
-        if constexpr (VEC) {
-          if (!(Tr::group_max(x[u]) >= tv)) continue;  // the common case: no candidate in the group
+          for (int o = 16; o > 0; o >>= 1)
+            lse_merge(mm, ss, __shfl_xor_sync(0xffffffffu, mm, o), __shfl_xor_sync(0xffffffffu, ss, o));
+          if (lane == 0) s_lse = mm + log2f(ss) * kLn2;
         }
-        float f[PV];
-        RV::floats(x[u], f);
+      }
+      __syncthreads();
+      prefix = (prefix << 8) | static_cast<uint32_t>(sel[0]);
+      need -= sel[1];
+    }
+    const uint32_t theta = prefix;
+
+    // ---------------- pass 2: every element with key >= theta, i.e. value >= theta's value
+    const float tv = Tr::kvalue(theta);
+    if (screen) {
+      // only the groups whose maximum reaches theta, listed first so that their
+      // re-reads (from L2) are all in flight together
+      // eight maxima per 16-byte read, compared as packed bf16 against the
+      // smallest bf16 >= theta's value
+      const __nv_bfloat162 th2 = __bfloat162bfloat162(__float2bfloat16_ru(tv));
+      const int nv = (ng + 7) / 8;
+      for (int v = tid; v < nv; v += CACHE_THREADS) {
+        const uint4 w = reinterpret_cast<const uint4*>(gmax)[v];
+        const uint32_t hit0 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.x & 0xFFFFu), __ushort_as_bfloat16(w.x >> 16)), th2);
+        const uint32_t hit1 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.y & 0xFFFFu), __ushort_as_bfloat16(w.y >> 16)), th2);
+        const uint32_t hit2 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.z & 0xFFFFu), __ushort_as_bfloat16(w.z >> 16)), th2);
+        const uint32_t hit3 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.w & 0xFFFFu), __ushort_as_bfloat16(w.w >> 16)), th2);
+        if (!(hit0 | hit1 | hit2 | hit3)) continue;  // the common case
+        const uint32_t hit[4] = {hit0, hit1, hit2, hit3};
 #pragma unroll
-        for (int i = 0; i < PV; ++i) {
-          if (f[i] >= tv) {
-            const int at = atomicAdd(&s_count, 1);
-            if (at < CACHE_CAP)
-              cand[at] = (static_cast<uint64_t>(~Tr::fkey(f[i])) << 32) | static_cast<uint32_t>(g * PV + i);
+        for (int e = 0; e < 8; ++e) {
+          const int g = v * 8 + e;
+          if (!((hit[e >> 1] >> (16 * (e & 1))) & 1u) || g >= ng) continue;
+          const int at = atomicAdd(&s_groups, 1);
+          if (at < CACHE_GLIST) {
+            glist[at] = g;
+          } else {  // a long list: this group now
+            float f[PV];
+            RV::floats(rv.load(g), f);
+#pragma unroll
+            for (int i = 0; i < PV; ++i)
+              if (f[i] >= tv) push_cand(cand, &s_count, Tr::fkey(f[i]), g * PV + i);
           }
+        }
+      }
+      __syncthreads();
+      const int nl = min(s_groups, CACHE_GLIST);
+      for (int i = tid; i < nl; i += CACHE_THREADS) {
+        const int g = glist[i];
+        float f[PV];
+        RV::floats(rv.load(g), f);
+#pragma unroll
+        for (int e = 0; e < PV; ++e)
+          if (f[e] >= tv) push_cand(cand, &s_count, Tr::fkey(f[e]), g * PV + e);
+      }
+    } else {
+      for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL) {
+        typename RV::Raw x[CACHE_UNROLL];
+#pragma unroll
+        for (int u = 0; u < CACHE_UNROLL; ++u)
+          if (g0 + u * CACHE_THREADS < ng) x[u] = rv.load(g0 + u * CACHE_THREADS);
+#pragma unroll
+        for (int u = 0; u < CACHE_UNROLL; ++u) {
+          const int g = g0 + u * CACHE_THREADS;
+          if (g >= ng) break;
+          if constexpr (VEC) {
+            if (!(Tr::group_max(x[u]) >= tv)) continue;  // the common case: no candidate in the group
+          }
+          float f[PV];
+          RV::floats(x[u], f);
+#pragma unroll
+          for (int i = 0; i < PV; ++i)
+            if (f[i] >= tv) push_cand(cand, &s_count, Tr::fkey(f[i]), g * PV + i);
         }
       }
     }
     if constexpr (VEC) {
       for (int j = ng * PV + tid; j < V; j += CACHE_THREADS) {
         const float f = Tr::value(rv.z[j]);
-        if (f >= tv) {
-          const int at = atomicAdd(&s_count, 1);
-          if (at < CACHE_CAP) cand[at] = (static_cast<uint64_t>(~Tr::fkey(f)) << 32) | static_cast<uint32_t>(j);
-        }
+        if (f >= tv) push_cand(cand, &s_count, Tr::fkey(f), j);
       }
     }
     __syncthreads();
@@ -317,9 +471,9 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       uint64_t lo2 = theta, hi2 = (Tr::KEY_BITS == 32) ? 0xFFFFFFFFull : 0xFFFFull;
       while (lo2 < hi2) {
         const uint64_t mid = lo2 + (hi2 - lo2 + 1) / 2;
-        int c = 0;
-        for (int j = tid; j < V; j += CACHE_THREADS) c += static_cast<uint64_t>(Tr::key(rv.z[j])) >= mid;
-        if (block_sum_int(c, red_i) >= K) lo2 = mid;
+        int cnt = 0;
+        for (int j = tid; j < V; j += CACHE_THREADS) cnt += static_cast<uint64_t>(Tr::key(rv.z[j])) >= mid;
+        if (block_sum_int(cnt, red_i) >= K) lo2 = mid;
         else hi2 = mid - 1;
       }
       const uint32_t kappa = static_cast<uint32_t>(lo2);
@@ -354,7 +508,24 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
     }
     // ---------------- order the candidates and emit the top K
     const float lse = s_lse;
-    if (n <= 2 * CACHE_THREADS) {
+    auto emit = [&](uint64_t c, int k) {
+      const float z = Tr::kvalue(~static_cast<uint32_t>(c >> 32));
+      idx_out[row * K + k] = static_cast<int>(c & 0xFFFFFFFFu);
+      p_out[row * K + k] = ex2((z - lse) * kLog2e);
+    };
+    if (n <= CACHE_THREADS / 2) {
+      // rank of each candidate = number of smaller composite keys (all distinct),
+      // counted by P lanes of one warp
+      int P = 1;
+      while (P < 32 && 2 * P * n <= CACHE_THREADS) P *= 2;
+      const int c = tid / P, part = tid % P;
+      const uint64_t mine = c < n ? cand[c] : ~0ull;
+      int rank = 0;
+      if (c < n)
+        for (int j = part; j < n; j += P) rank += cand[j] < mine;
+      for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+      if (c < n && part == 0 && rank < K) emit(mine, rank);
+    } else if (n <= 2 * CACHE_THREADS) {
       // rank of each candidate = number of smaller composite keys (all distinct)
       uint64_t mine[2];
       int rank[2] = {0, 0};
@@ -363,33 +534,24 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       if (tid < n) {  // only candidate owners count
         if (tid + CACHE_THREADS < n) {
           for (int j = 0; j < n; ++j) {
-            const uint64_t c = cand[j];
-            rank[0] += c < mine[0];
-            rank[1] += c < mine[1];
+            const uint64_t cj = cand[j];
+            rank[0] += cj < mine[0];
+            rank[1] += cj < mine[1];
           }
         } else {
           for (int j = 0; j < n; ++j) rank[0] += cand[j] < mine[0];
         }
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (tid + h * CACHE_THREADS < n && rank[h] < K) {
-          const int id = static_cast<int>(mine[h] & 0xFFFFFFFFu);
-          idx_out[row * K + rank[h]] = id;
-          p_out[row * K + rank[h]] = ex2((Tr::value(rv.z[id]) - lse) * kLog2e);
-        }
-      }
+      for (int h = 0; h < 2; ++h)
+        if (tid + h * CACHE_THREADS < n && rank[h] < K) emit(mine[h], rank[h]);
     } else {
       int n_pad = 1;
       while (n_pad < n) n_pad <<= 1;
       for (int i = n + tid; i < n_pad; i += CACHE_THREADS) cand[i] = ~0ull;
       __syncthreads();
       block_bitonic_sort_u64(cand, n_pad);
-      for (int k = tid; k < K; k += CACHE_THREADS) {
-        const int id = static_cast<int>(cand[k] & 0xFFFFFFFFu);
-        idx_out[row * K + k] = id;
-        p_out[row * K + k] = ex2((Tr::value(rv.z[id]) - lse) * kLog2e);
-      }
+      for (int k = tid; k < K; k += CACHE_THREADS) emit(cand[k], k);
     }
     if (tid == 0 && lse_out) lse_out[row] = lse;
   }

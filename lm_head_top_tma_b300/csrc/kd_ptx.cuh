@@ -91,6 +91,16 @@ __device__ __forceinline__ bool mbar_wait_quiet(uint32_t bar, uint32_t parity, u
 }
 
 // ------------------------------------------------------------------ TMA
+// Prefetch [p, p + bytes) into L2 (cp.async.bulk.prefetch.L2): p 16-byte
+// aligned, bytes a multiple of 16; issued in pieces of at most 64 KB.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, int64_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (; bytes > 0; bytes -= 65536, c += 65536) {
+    const uint32_t n = bytes > 65536 ? 65536u : static_cast<uint32_t>(bytes);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c), "r"(n) : "memory");
+  }
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }

@@ -611,14 +611,17 @@ kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, in
   const int sms = current_sm_count();
   const int slot = prof_begin(KD_K_OTHER, st);
   cudaError_t e = cudaSuccess;
+  const int smem = cache_smem_bytes(vec);
   auto run_kernel = [&](auto kern, const auto* z) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CACHE_THREADS, 0) != cudaSuccess || per_sm < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CACHE_THREADS, smem) != cudaSuccess || per_sm < 1) {
       cudaGetLastError();
       per_sm = 1;
     }
     const int blocks = static_cast<int>(std::min<int64_t>(T, int64_t(per_sm) * sms));
-    kern<<<blocks, CACHE_THREADS, 0, st>>>(z, T, V, K, idx, p, lse);
+    kern<<<blocks, CACHE_THREADS, smem, st>>>(z, T, V, K, idx, p, lse);
     e = cudaGetLastError();
   };
   if (logits_bf16) {

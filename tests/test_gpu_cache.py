@@ -10,7 +10,13 @@ sum moves p by ~1/V relative only for flat rows, but a missing max-shift,
 a wrong base or a wrong id moves it by orders of magnitude).  Cases: teacher-
 like bf16 and fp32 rows at the workloads' vocabulary sizes, V below the block
 size, K = 1, K = V, K = 1024, heavily tied rows, rows that force the exact
-fallback (thousands of equal maxima, all-equal rows), and masked -inf logits."""
+fallback (thousands of equal maxima, all-equal rows), and masked -inf logits.
+The builder keeps every 16-byte group's maximum in shared memory (up to 32768
+groups: bf16 rows up to V = 262144, fp32 rows up to V = 131072) and re-reads
+only the groups that can hold a top-K element; the placement cases put the
+top K at the row's end, its start, in one run, scattered, and the capacity
+cases take rows at and just past the largest V it covers (longer rows are
+scanned whole)."""
 import numpy as np
 import pytest
 import torch
@@ -50,7 +56,7 @@ def test_teacher_like_rows(cuda_device, dtype, V, K):
 
 @pytest.mark.parametrize("T,V,K", [(5, 300, 5), (3, 64, 64), (7, 1000, 1), (4, 5000, 1024), (2, 1024, 1024),
                                    (1, 1, 1), (9, 2047, 33),
-                                   (3000, 520, 7),       # many short rows per block through the copy ring
+                                   (3000, 520, 7),       # many short rows per block
                                    (700, 16392, 100)])   # rows of two chunks, the second nearly empty
 def test_shapes(cuda_device, T, V, K):
     Z = make_teacher_logits(T, V, seed=T * V + K, device=cuda_device, dtype="bf16")
@@ -96,3 +102,43 @@ def test_full_size_sampled_rows(cuda_device):
     Z = make_teacher_logits(2048, 128256, seed=5, device=cuda_device, dtype="bf16")
     rng = np.random.default_rng(0)
     check(Z, 100, rows=np.sort(rng.choice(2048, 48, replace=False)))
+
+
+GMAX_GROUPS = 32768  # 16-byte group maxima kept in shared memory
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_topk_placement(cuda_device, dtype):
+    """Top K at the row's end, at its start, in one run of 120 ids, K equal
+    maxima scattered, and one half of the row uniformly above the other."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    V, K = 128256, 100
+    mid = V // 4
+    Z = make_teacher_logits(6, V, seed=21, device=cuda_device, dtype=dtype)
+    g = torch.Generator(device="cpu").manual_seed(3)
+    ramp = torch.linspace(-20.0, 20.0, V)
+    Z[0] = ramp.to(tdt).to(cuda_device)                             # ascending: top K at the row's end
+    Z[1] = ramp.flip(0).to(tdt).to(cuda_device)                     # descending: top K at its start
+    Z[2, mid - 60:mid + 60] = (8.0 + torch.rand(120, generator=g)).to(tdt).to(cuda_device)
+    Z[3, torch.randperm(V, generator=g)[:K].to(cuda_device)] = 9.0  # K equal maxima anywhere
+    Z[4, mid:] = Z[4, mid:] + 3.0
+    Z[5, :mid] = Z[5, :mid] + 3.0
+    check(Z, K)
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", GMAX_GROUPS * 8), ("bf16", GMAX_GROUPS * 8 + 8),
+                                     ("bf16", GMAX_GROUPS * 8 - 3), ("fp32", GMAX_GROUPS * 4),
+                                     ("fp32", GMAX_GROUPS * 4 + 4)])
+def test_rows_around_group_maxima_capacity(cuda_device, dtype, V):
+    """Rows with exactly as many 16-byte groups as shared memory holds maxima
+    for, one group more (scanned whole), and a bf16 row just short of it whose
+    length is not a multiple of 16 bytes (element-wise loads)."""
+    Z = make_teacher_logits(6, V, seed=V, device=cuda_device, dtype=dtype)
+    check(Z, 100)
+
+
+@pytest.mark.parametrize("K", [1, 16, 17, 512, 1024])
+def test_k_values_full_vocab(cuda_device, K):
+    """K from 1 to the largest supported, on rows of the benchmark's vocabulary."""
+    Z = make_teacher_logits(12, 128256, seed=K, device=cuda_device, dtype="bf16")
+    check(Z, K)
