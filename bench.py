@@ -47,10 +47,10 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 # of two 2048-row chunks, the first group of a step stores dW ("first"), the
 # others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
 # chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": "fae53b511ca64e08", "kinds": {
-    "gemm_dw": {"first": 1362949888 + 1544164096, "rest": 2755587584 + 1536736512},
-    "logits_gf": {"first": 1126369536 + 522738432,
-                  "rest": (864735744 + 522315776 + 911572224 + 522344192) // 2},
+TRAFFIC = {"workload": "longctx", "src_sha": "447ff2ed5d182d78", "kinds": {
+    "gemm_dw": {"first": 1515243520 + 1545350912, "rest": 2793174528 + 1538373632},
+    "logits_gf": {"first": 916718592 + 522833920,
+                  "rest": (880588288 + 523105024 + 897105152 + 522820864) // 2},
 }}
 KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300/csrc/kd_ptx.cuh",
                   "lm_head_top_tma_b300/csrc/kdtopk.cu"]
