@@ -168,7 +168,7 @@ struct RowView {
   int V;
   static constexpr int PV = VEC ? LogitTraits<TL>::PER_VEC : 1;
   using Raw = typename std::conditional<VEC, uint4, TL>::type;
-  __device__ int groups() const { return VEC ? V / PV : V; }
+  __device__ int groups() const { return VEC ? V / PV : V; }  // VEC rows are whole 16-byte groups
   __device__ Raw load(int g) const {
     if constexpr (VEC) return __ldg(reinterpret_cast<const uint4*>(z) + g);
     else return z[g];
@@ -347,13 +347,7 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
         }
       }
     }
-    if constexpr (VEC) {  // the tail that does not fill a 16-byte vector
-      for (int j = ng * PV + tid; j < V; j += CACHE_THREADS) {
-        const TL x[1] = {rv.z[j]};
-        float gm[1];
-        groups_stats<1, RowView<TL, false>>(x, gm, m, s, fslot1);
-      }
-    }
+    // (rows read 16 bytes at a time are whole groups: there is no tail)
     // slots without elements hold -inf: no larger than any element, so they never raise theta
     const uint32_t kslot0 = Tr::fkey(fslot0), kslot1 = Tr::fkey(fslot1);
 #pragma unroll
@@ -455,12 +449,6 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
           for (int i = 0; i < PV; ++i)
             if (f[i] >= tv) push_cand(cand, &s_count, Tr::fkey(f[i]), g * PV + i);
         }
-      }
-    }
-    if constexpr (VEC) {
-      for (int j = ng * PV + tid; j < V; j += CACHE_THREADS) {
-        const float f = Tr::value(rv.z[j]);
-        if (f >= tv) push_cand(cand, &s_count, Tr::fkey(f), j);
       }
     }
     __syncthreads();
