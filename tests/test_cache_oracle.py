@@ -2,7 +2,9 @@
 things other than itself: closed forms (strictly decreasing logits: a
 geometric series; equal logits: the first K ids at 1/V each), invariants
 (logit shift, K = V gives the whole distribution), brute force against the
-pure-Python selection on tiny tied inputs, and torch.topk's values."""
+pure-Python selection on tiny tied inputs, and torch.topk's values.  The last
+test plants plausible mistakes in a copy of the oracle and checks that the
+pins reject each one."""
 import math
 
 import numpy as np
@@ -76,3 +78,63 @@ def test_values_match_torch_topk():
     assert np.array_equal(got, vals)
     lse = torch.logsumexp(Z.double(), dim=1).numpy()
     np.testing.assert_allclose(out["lse"], lse, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- pin sensitivity
+def _pins(fn):
+    """The pins above as checks of a cache function fn(Z, K) -> {idx, p, lse};
+    returns the names of the pins it fails."""
+    failed = []
+    V, K, a = 50, 7, 0.3
+    out = fn(-a * np.arange(V, dtype=np.float64)[None, :], K)
+    ref = [math.exp(-k * a) * (1 - math.exp(-a)) / (1 - math.exp(-V * a)) for k in range(K)]
+    if out["idx"][0].tolist() != list(range(K)) or not np.allclose(out["p"][0], ref, rtol=1e-12):
+        failed.append("geometric closed form")
+    out = fn(np.full((1, 40), 1.75), 9)
+    if out["idx"][0].tolist() != list(range(9)) or not np.allclose(out["p"], 1 / 40, rtol=1e-12):
+        failed.append("equal logits")
+    Z = make_teacher_logits(4, 300, seed=5).float()
+    out = fn(Z, 20)
+    vals = torch.topk(Z.double(), 20, dim=1).values.numpy()
+    got = np.take_along_axis(Z.double().numpy(), out["idx"].astype(np.int64), axis=1)
+    if not np.array_equal(got, vals) or not np.allclose(out["lse"], torch.logsumexp(Z.double(), 1).numpy(),
+                                                          rtol=1e-12):
+        failed.append("torch.topk values and logsumexp")
+    Zt = make_teacher_logits(3, 23, seed=1, noise=0.5).float().numpy()
+    Zt[:, ::4] = Zt[:, 2:3]
+    a_, b_ = fn(Zt, 6), topk_cache_naive(Zt, 6)
+    if not np.array_equal(a_["idx"], b_["idx"]) or not np.allclose(a_["p"], b_["p"], rtol=1e-12):
+        failed.append("brute force")
+    return failed
+
+
+def _variant(mistake):
+    """topk_cache_oracle with one plausible mistake planted (CPU, test-local)."""
+    def fn(Z, K):
+        Z = np.asarray(Z.double().numpy() if hasattr(Z, "double") else Z, dtype=np.float64)
+        T, V = Z.shape
+        ids = np.arange(V)
+        idx = np.empty((T, K), dtype=np.int32)
+        p = np.empty((T, K))
+        lse = np.empty(T)
+        for t in range(T):
+            z = Z[t]
+            order = np.lexsort((-ids if mistake == "ties by descending id" else ids, -z))
+            if mistake == "ascending order":
+                order = np.lexsort((ids, z))
+            idx[t] = order[1:K + 1] if mistake == "off by one rank" and V > K else order[:K]
+            m = z.max()
+            terms = z[idx[t]] if mistake == "lse over the top K" else z
+            lse[t] = m + math.log(np.exp(terms - m).sum())
+            p[t] = np.exp(z[idx[t]] - lse[t])
+            if mistake == "p renormalised over the top K":
+                p[t] /= p[t].sum()
+        return {"idx": idx, "p": p, "lse": lse}
+    return fn
+
+
+def test_pins_catch_planted_mistakes():
+    assert _pins(topk_cache_oracle) == []
+    for mistake in ("ties by descending id", "ascending order", "off by one rank", "lse over the top K",
+                    "p renormalised over the top K"):
+        assert _pins(_variant(mistake)), mistake
