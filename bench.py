@@ -20,7 +20,8 @@ inputs resident in HBM; ``e2e`` repeats the measurement through the public
 API with the step's inputs (H, idx, p) copied from pinned host memory (on a
 side stream, one step ahead, into two device buffers) and the loss read back
 every step; ``variants.fused_norecompute`` times the fused step without the
-backward recompute in the same run.  N > 1 runs one independent replica per
+backward recompute in the same run, and ``variants.separate_forward_backward``
+the forward and backward entry points called one after the other.  N > 1 runs one independent replica per
 GPU (torchrun; the path needs no data exchange for this metric), timed
 between barriers, max over ranks.
 """
@@ -410,6 +411,34 @@ def run_kdtopk(args):
             "per_kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof_nr.items() if v[1]},
             "launches_per_step": {k: v[1] // args.steps for k, v in prof_nr.items() if v[1]},
             "clocks": clk_nr}
+
+        # ---- forward and backward as separate calls (kd_topk_kl_forward, then
+        # kd_topk_kl_backward with the saved lse), each timed over its own loop
+        dW_sep = torch.empty(V, d, dtype=torch.float32, device=dev)
+        lse_sep = api.forward(H, W, idx, p, C, workspace=work, check=False)[1]
+        for _ in range(args.warmup):
+            api.forward(H, W, idx, p, C, workspace=work, check=False)
+            api.backward(H, W, idx, p, lse_sep, C, dW=dW_sep, workspace=work, check=False)
+        ms_sep = {}
+        for name, call in (("forward", lambda: api.forward(H, W, idx, p, C, workspace=work, check=False)),
+                           ("backward", lambda: api.backward(H, W, idx, p, lse_sep, C, dW=dW_sep, workspace=work,
+                                                             check=False))):
+            barrier(ws)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for _ in range(args.steps):
+                call()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier(ws)
+            ms_sep[name] = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws)
+        N.check(api.device_status(work.buf, dev), "separate forward / backward calls")
+        ms_fb = ms_sep["forward"] + ms_sep["backward"]
+        variants["separate_forward_backward"] = {
+            "value": ws * T / (ms_fb / 1e3), "unit": "tokens/s", "ms_per_step": ms_fb,
+            "forward_ms": ms_sep["forward"], "backward_ms": ms_sep["backward"],
+            "tflops_8TVd": ws * 8.0 * T * V * d / (ms_fb / 1e3) / 1e12}
+        del dW_sep
 
     flops_8 = 8.0 * T * V * d
     flops_6 = 6.0 * T * V * d
