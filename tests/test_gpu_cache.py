@@ -142,3 +142,23 @@ def test_k_values_full_vocab(cuda_device, K):
     """K from 1 to the largest supported, on rows of the benchmark's vocabulary."""
     Z = make_teacher_logits(12, 128256, seed=K, device=cuda_device, dtype="bf16")
     check(Z, K)
+
+
+def test_cache_feeds_the_loss(cuda_device):
+    """The offline step and the loss together: the cache the GPU builds from
+    teacher logits drives the fused step; the reference runs the oracle's cache
+    through the loss oracle.  Chunks of 128 rows (pair GEMMs off) and 256
+    (on), with a ragged last chunk."""
+    from parity_util import assert_close_full, fused_to_host, kd_oracle
+    from lm_head_top_tma_b300.inputs import make_hw
+
+    T, d, V, K = 300, 256, 4096, 32
+    Z = make_teacher_logits(T, V, seed=31, device=cuda_device, dtype="bf16")
+    idx, p, _ = api.topk_cache_build(Z, K)
+    ref_cache = topk_cache_oracle(Z.cpu(), K)
+    assert np.array_equal(idx.cpu().numpy(), ref_cache["idx"])
+    H, W = make_hw(T, d, V, "zipf", seed=5, device=cuda_device)
+    ref = kd_oracle(H.cpu(), W.cpu(), ref_cache["idx"], ref_cache["p"])
+    for chunk in (128, 256):
+        got = fused_to_host(api.fused_step(H, W, idx, p, chunk, loss_rows=True))
+        assert_close_full(got, ref)
