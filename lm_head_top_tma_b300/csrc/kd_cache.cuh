@@ -509,8 +509,10 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       const int c = tid / P, part = tid % P;
       const uint64_t mine = c < n ? cand[c] : ~0ull;
       int rank = 0;
-      if (c < n)
+      if (c < n) {
+#pragma unroll 4
         for (int j = part; j < n; j += P) rank += cand[j] < mine;
+      }
       for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
       if (c < n && part == 0 && rank < K) emit(mine, rank);
     } else if (n <= 2 * CACHE_THREADS) {
