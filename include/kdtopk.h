@@ -201,7 +201,8 @@ KD_API kd_status kd_topk_kl_forward_noalloc(const void* H, const void* W, const 
  *                 (fp32, device, [T, K]); the row mass sum_k p <= 1;
  *   lse[t]        log sum_j exp(z_tj) (fp32, device, [T]; may be NULL).
  * Temperature 1; -0 and +0 are equal logits; -inf logits carry no
- * probability.  1 <= K <= min(V, 1024) (KD_ERR_INVALID_ARG /
+ * probability; NaN logits are not supported (their rank and the row's p and
+ * lse are unspecified).  1 <= K <= min(V, 1024) (KD_ERR_INVALID_ARG /
  * KD_ERR_UNSUPPORTED otherwise).  Rows whose length in bytes is a multiple
  * of 16 (with a 16-byte aligned base) are read with 16-byte loads, others
  * element by element.  Allocates nothing, waits on nothing (no device-side
