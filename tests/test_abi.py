@@ -96,3 +96,9 @@ def test_workspace_is_flat_in_T(lib):
         lib.kd_topk_kl_workspace_size(100, 256, 4096, 16, 100, 3)
     assert lib.kd_topk_kl_workspace_size(0, 256, 4096, 16, 64, 3) == 0
     assert lib.kd_topk_kl_workspace_size(256, 250, 4096, 16, 64, 3) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No fallback: a library that is not there is an error, not a slower path."""
+    with pytest.raises(RuntimeError, match="not found"):
+        N.load(str(tmp_path / "libkdtopk.so"))
