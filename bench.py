@@ -556,8 +556,9 @@ def run_sweep(args):
 
 def run_topk_cache(args):
     """Teacher-cache builder: top-K ids and probabilities of every row of
-    synthetic teacher logits Z [T, V] (bf16), one JSON line.  HBM-bound: the
-    algorithmic bytes are one read of Z plus the cache written (idx, p, lse)."""
+    synthetic teacher logits Z [T, V] (bf16, or fp32 with --logits-dtype fp32),
+    one JSON line.  HBM-bound: the algorithmic bytes are one read of Z plus the
+    cache written (idx, p, lse)."""
     import torch
 
     from lm_head_top_tma_b300 import api
@@ -566,7 +567,7 @@ def run_topk_cache(args):
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     T, V, K = args.T or 32768, 128256, 100
-    Z = make_teacher_logits(T, V, seed=7, device=dev, dtype="bf16")
+    Z = make_teacher_logits(T, V, seed=7, device=dev, dtype=args.logits_dtype)
     for _ in range(max(3, args.warmup)):
         api.topk_cache_build(Z, K)
     torch.cuda.synchronize(dev)
@@ -587,13 +588,13 @@ def run_topk_cache(args):
     api.profile_enable(False)
     ms = e0.elapsed_time(e1) / args.steps
     kern_ms, kern_n = prof["other"]
-    bytes_alg = T * V * 2 + T * K * 8 + T * 4
+    bytes_alg = T * V * Z.element_size() + T * K * 8 + T * 4
     peaks = load_peaks()
     achieved = bytes_alg / (kern_ms / kern_n / 1e3) / 1e9
     print(json.dumps({
         "metric": "teacher top-K cache build rows/s", "value": T / (ms / 1e3), "unit": "rows/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "dtype": "bf16", "data": "synthetic", "config": {"workload": "teacher_logits", "T": T, "V": V, "K": K,
+        "dtype": args.logits_dtype, "data": "synthetic", "config": {"workload": "teacher_logits", "T": T, "V": V, "K": K,
                                                           "l2": "logits larger than L2, no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm"], "traffic": None, "bytes_per_launch": bytes_alg},
@@ -614,6 +615,8 @@ def main():
     ap.add_argument("--no-variants", action="store_true", help="skip the no-recompute fused step timing")
     ap.add_argument("--sweep", action="store_true", help="output-head-only T sweep, one line per T")
     ap.add_argument("--topk-cache", action="store_true", help="teacher-cache builder over synthetic logits")
+    ap.add_argument("--logits-dtype", default="bf16", choices=["bf16", "fp32"],
+                    help="teacher logits' type for --topk-cache")
     args = ap.parse_args()
     if args.sweep:
         return run_sweep(args)
