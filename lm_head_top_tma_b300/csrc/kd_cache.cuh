@@ -195,6 +195,23 @@ __device__ __forceinline__ void push_cand(uint64_t* cand, int* count, uint32_t k
   if (at < CACHE_CAP) cand[at] = (static_cast<uint64_t>(~key) << 32) | static_cast<uint32_t>(id);
 }
 
+// Reserves n >= 0 consecutive slots of a shared counter for each lane of the
+// warp (all 32 lanes call it) with one atomic per warp; returns the lane's
+// first slot.
+__device__ __forceinline__ int warp_reserve(int* counter, int n) {
+  const int lane = threadIdx.x & 31;
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  int base = 0;
+  if (lane == 31 && total) base = atomicAdd(counter, total);
+  return __shfl_sync(0xffffffffu, base, 31) + incl - n;
+}
+
 // One byte-level step of a most-significant-byte-first radix select of the
 // K-th largest of the block's 2 * CACHE_THREADS keys (two per thread), after
 // every thread has counted its keys that share `prefix` into hist[256] by the
@@ -396,19 +413,23 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       // smallest bf16 >= theta's value
       const __nv_bfloat162 th2 = __bfloat162bfloat162(__float2bfloat16_ru(tv));
       const int nv = (ng + 7) / 8;
-      for (int v = tid; v < nv; v += CACHE_THREADS) {
-        const uint4 w = reinterpret_cast<const uint4*>(gmax)[v];
-        const uint32_t hit0 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.x & 0xFFFFu), __ushort_as_bfloat16(w.x >> 16)), th2);
-        const uint32_t hit1 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.y & 0xFFFFu), __ushort_as_bfloat16(w.y >> 16)), th2);
-        const uint32_t hit2 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.z & 0xFFFFu), __ushort_as_bfloat16(w.z >> 16)), th2);
-        const uint32_t hit3 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.w & 0xFFFFu), __ushort_as_bfloat16(w.w >> 16)), th2);
-        if (!(hit0 | hit1 | hit2 | hit3)) continue;  // the common case
-        const uint32_t hit[4] = {hit0, hit1, hit2, hit3};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int g = v * 8 + e;
-          if (!((hit[e >> 1] >> (16 * (e & 1))) & 1u) || g >= ng) continue;
-          const int at = atomicAdd(&s_groups, 1);
+      for (int v0 = warp * 32; v0 < nv; v0 += CACHE_THREADS) {  // v = tid + k CACHE_THREADS
+        const int v = v0 + lane;
+        uint32_t m8 = 0;  // bit e: group v * 8 + e reaches theta
+        if (v < nv) {
+          const uint4 w = reinterpret_cast<const uint4*>(gmax)[v];
+          const uint32_t h0 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.x & 0xFFFFu), __ushort_as_bfloat16(w.x >> 16)), th2);
+          const uint32_t h1 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.y & 0xFFFFu), __ushort_as_bfloat16(w.y >> 16)), th2);
+          const uint32_t h2 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.z & 0xFFFFu), __ushort_as_bfloat16(w.z >> 16)), th2);
+          const uint32_t h3 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.w & 0xFFFFu), __ushort_as_bfloat16(w.w >> 16)), th2);
+          m8 = (h0 & 1u) | ((h0 >> 15) & 2u) | ((h1 & 1u) << 2) | ((h1 >> 13) & 8u) | ((h2 & 1u) << 4) |
+               ((h2 >> 11) & 32u) | ((h3 & 1u) << 6) | ((h3 >> 9) & 128u);
+          if (v * 8 + 8 > ng) m8 &= (1u << (ng - v * 8)) - 1u;  // groups past the row's end
+        }
+        if (!__any_sync(0xffffffffu, m8 != 0)) continue;  // the common case
+        int at = warp_reserve(&s_groups, __popc(m8));
+        for (; m8; m8 &= m8 - 1u, ++at) {
+          const int g = v * 8 + __ffs(m8) - 1;
           if (at < CACHE_GLIST) {
             glist[at] = g;
           } else {  // a long list: this group now
@@ -422,13 +443,23 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       }
       __syncthreads();
       const int nl = min(s_groups, CACHE_GLIST);
-      for (int i = tid; i < nl; i += CACHE_THREADS) {
-        const int g = glist[i];
+      for (int i0 = warp * 32; i0 < nl; i0 += CACHE_THREADS) {  // i = tid + k CACHE_THREADS
+        const int i = i0 + lane;
+        const int g = i < nl ? glist[i] : 0;
         float f[PV];
-        RV::floats(rv.load(g), f);
+        uint32_t mk = 0;  // bit e: element e of the group reaches theta
+        if (i < nl) {
+          RV::floats(rv.load(g), f);
+#pragma unroll
+          for (int e = 0; e < PV; ++e) mk |= static_cast<uint32_t>(f[e] >= tv) << e;
+        }
+        int at = warp_reserve(&s_count, __popc(mk));
 #pragma unroll
         for (int e = 0; e < PV; ++e)
-          if (f[e] >= tv) push_cand(cand, &s_count, Tr::fkey(f[e]), g * PV + e);
+          if ((mk >> e) & 1u) {
+            if (at < CACHE_CAP) cand[at] = (static_cast<uint64_t>(~Tr::fkey(f[e])) << 32) | static_cast<uint32_t>(g * PV + e);
+            ++at;
+          }
       }
     } else {
       for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL) {
