@@ -13,13 +13,16 @@
 //           exactly one), an online (max, sum of 2^x) for lse, and the maximum
 //           of every 16-byte group, kept in shared memory (as bf16, rounded up
 //           for fp32 logits);
-//   select  theta = the K-th largest slot maximum, by a binary search over the
-//           key space with block-wide counts: at least K distinct elements
-//           reach theta, so every top-K element has key >= theta;
+//   select  theta = the K-th largest slot maximum, by a byte-wise radix select
+//           over 256-bin shared-memory histograms (with the block's lse
+//           reduced alongside): at least K distinct elements reach theta, so
+//           every top-K element has key >= theta;
 //   pass 2  only the groups whose maximum reaches theta (typically about K of
-//           them) are read again, from L2, and their elements >= theta are
-//           collected in shared memory; they are ranked by (key descending,
-//           id ascending) by counting (bitonic sort above 1024 candidates);
+//           them) are listed and read again, from L2, all in flight together,
+//           and their elements >= theta are collected in shared memory (list
+//           and candidates appended with one atomic per warp); they are
+//           ranked by (key descending, id ascending) by counting (bitonic
+//           sort above 1024 candidates);
 //   fallback  rows whose group maxima do not fit in shared memory, or that
 //           cannot be read 16 bytes at a time, are scanned whole in pass 2;
 //           when more than CACHE_CAP elements reach theta (heavily tied or
