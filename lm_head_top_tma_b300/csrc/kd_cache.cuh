@@ -8,7 +8,9 @@
 //
 // One block of 512 threads per row (grid-stride over rows, two blocks per
 // SM); each row is read from HBM once, with 16-byte loads, several in flight
-// per thread, after an L2 prefetch of the whole row:
+// per thread, after an L2 prefetch of the whole row (its first 64 KB already
+// prefetched while the block selected its previous row, so that HBM keeps
+// streaming through the selection; more than that crowds L2):
 //   pass 1  per-slot maximum (1024 slots: two per thread, every element in
 //           exactly one), an online (max, sum of 2^x) for lse, and the maximum
 //           of every 16-byte group, kept in shared memory (as bf16, rounded up
@@ -406,6 +408,12 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       need -= sel[1];
     }
     const uint32_t theta = prefix;
+    if constexpr (VEC) {
+      // the head of the block's next row into L2 while this row's selection runs
+      if (tid == 0 && row + gridDim.x < T)
+        prefetch_l2_bulk(rv.z + static_cast<int64_t>(gridDim.x) * V,
+                         min(static_cast<int64_t>(V) * static_cast<int64_t>(sizeof(TL)), int64_t(65536)));
+    }
 
     // ---------------- pass 2: every element with key >= theta, i.e. value >= theta's value
     const float tv = Tr::kvalue(theta);
