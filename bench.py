@@ -48,7 +48,7 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 # of two 2048-row chunks, the first group of a step stores dW ("first"), the
 # others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
 # chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": "447ff2ed5d182d78", "kinds": {
+TRAFFIC = {"workload": "longctx", "src_sha": "4686b7befbdcac5d", "kinds": {
     "gemm_dw": {"first": 1515243520 + 1545350912, "rest": 2793174528 + 1538373632},
     "logits_gf": {"first": 916718592 + 522833920,
                   "rest": (880588288 + 523105024 + 897105152 + 522820864) // 2},
