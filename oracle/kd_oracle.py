@@ -50,7 +50,7 @@ import math
 
 import numpy as np
 
-__all__ = ["kd_oracle", "kd_oracle_rows", "kd_oracle_naive", "valid_rows"]
+__all__ = ["kd_oracle", "kd_oracle_rows", "kd_oracle_dW_rows", "kd_oracle_naive", "valid_rows"]
 
 
 def _f64(a) -> np.ndarray:
@@ -130,6 +130,49 @@ def kd_oracle_rows(H, W, idx, p, rows, rows_per_block: int = 256):
     out = kd_oracle(Hs, W, np.asarray(idx)[rows], np.asarray(p)[rows],
                     want_grads=True, rows_per_block=rows_per_block)
     return {"rows": rows, "lse": out["lse"], "loss_rows": out["loss_rows"], "dH": out["dH"]}
+
+
+def kd_oracle_dW_rows(H, W, idx, p, lse, vrows, rows_per_block: int = 1024):
+    """Selected vocabulary rows of dW = G^T H, given lse_t for every token.
+
+    dW_j = sum_t G_tj H_t with G_tj = M_t exp(z_tj - lse_t) - sum_{k: idx_tk = j}
+    p_tk, the same G as ``kd_oracle`` (legiblepapers FAQ Q5 gradient), taken
+    column by column: only z_tj = H_t . W_j for the selected j is formed, so a
+    test can check chosen rows of dW for a sequence too long for the full fp64
+    backward.  ``lse`` must be the oracle's own (``kd_oracle`` with
+    ``want_grads=False``) for all T rows; rows with an id outside [0, V)
+    contribute nothing.  ``vrows`` are distinct vocabulary ids; returns
+    [len(vrows), d]."""
+    Wd = _f64(W)
+    idx = np.asarray(idx).astype(np.int64)
+    pd = _f64(p)
+    lse = np.asarray(lse, dtype=np.float64)
+    vrows = np.asarray(vrows, dtype=np.int64)
+    if np.unique(vrows).size != vrows.size:
+        raise ValueError("vrows must be distinct")
+    T, K = idx.shape
+    V, d = Wd.shape
+    ok = valid_rows(idx, V)
+    col = np.full(V, -1, dtype=np.int64)                     # vocabulary id -> selected column
+    col[vrows] = np.arange(vrows.size)
+    Wj = Wd[vrows]                                           # [J, d]
+    out = np.zeros((vrows.size, d))
+    for t0 in range(0, T, rows_per_block):
+        t1 = min(T, t0 + rows_per_block)
+        Hb = _f64(H[t0:t1])
+        zJ = Hb @ Wj.T                                       # [B, J]
+        ib = idx[t0:t1]
+        pb = pd[t0:t1]
+        M = pb.sum(axis=1)
+        G = M[:, None] * np.exp(zJ - lse[t0:t1, None])
+        ib_safe = np.where(ok[t0:t1, None], ib, 0)
+        c = col[ib_safe]                                     # [B, K], -1 where the id is not selected
+        hit = c >= 0
+        rows = np.repeat(np.arange(t1 - t0)[:, None], K, axis=1)
+        np.subtract.at(G, (rows[hit], c[hit]), pb[hit])
+        G[~ok[t0:t1]] = 0.0
+        out += G.T @ Hb
+    return out
 
 
 def kd_oracle_naive(H, W, idx, p):

@@ -21,7 +21,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import kd_oracle, kd_oracle_naive, kd_oracle_rows
+from oracle import kd_oracle, kd_oracle_dW_rows, kd_oracle_naive, kd_oracle_rows
 from lm_head_top_tma_b300.inputs import make_cache, make_hw, make_inputs
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
@@ -245,6 +245,63 @@ def test_rows_subset_matches_full():
     np.testing.assert_allclose(sub["lse"], full["lse"][rows], atol=1e-13)
     np.testing.assert_allclose(sub["loss_rows"], full["loss_rows"][rows], atol=1e-13)
     np.testing.assert_allclose(sub["dH"], full["dH"][rows], atol=1e-13)
+
+
+def test_dW_rows_finite_differences():
+    """Selected rows of dW from the oracle's own lse equal central finite
+    differences of L with respect to those rows of W (duplicates, pads and a
+    zero-mass row included), independently of the full backward."""
+    H, W, idx, p = _rand_case(4, 6, 14, 5, seed=31, distinct=False)
+    idx[0, 1] = idx[0, 0]
+    p[1, 2] = 0.0
+    p[2, :] = 0.0
+    lse = kd_oracle(H, W, idx, p, want_grads=False)["lse"]
+    vrows = np.array([13, 0, int(idx[0, 0]) if idx[0, 0] not in (13, 0) else 5, 7])
+    got = kd_oracle_dW_rows(H, W, idx, p, lse, vrows, rows_per_block=3)
+    h = 1e-6
+    num = np.zeros((len(vrows), W.shape[1]))
+    for a, j in enumerate(vrows):
+        for c in range(W.shape[1]):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[j, c] += h
+            Wm[j, c] -= h
+            num[a, c] = (_loss_only(H, Wp, idx, p) - _loss_only(H, Wm, idx, p)) / (2 * h)
+    assert np.abs(got - num).max() <= 1e-7 * max(np.abs(num).max(), 1.0)
+
+
+def test_dW_rows_match_full_backward():
+    T, d, V, K = 11, 5, 40, 6
+    H, W, idx, p = _rand_case(T, d, V, K, seed=32, distinct=False)
+    idx[0, 1] = idx[0, 0]          # duplicate id
+    idx[1, :] = 39                 # one id K times, at the vocabulary end
+    p[2, 3] = 0.0                  # zero-probability pad
+    p[3, :] = 0.0                  # no teacher mass
+    idx[4, 2] = V + 1              # bad id: the row contributes nothing
+    idx[5, 0] = -2
+    full = kd_oracle(H, W, idx, p)
+    vrows = np.array([39, 0, int(idx[0, 0]), 17, 38]) if idx[0, 0] not in (39, 0, 17, 38) else np.array([39, 0, 17, 38])
+    for rpb in (1, 4, 1024):
+        got = kd_oracle_dW_rows(H, W, idx, p, full["lse"], vrows, rows_per_block=rpb)
+        np.testing.assert_allclose(got, full["dW"][vrows], atol=1e-13)
+    all_rows = kd_oracle_dW_rows(H, W, idx, p, full["lse"], np.arange(V))
+    np.testing.assert_allclose(all_rows, full["dW"], atol=1e-13)
+    with pytest.raises(ValueError):
+        kd_oracle_dW_rows(H, W, idx, p, full["lse"], np.array([3, 3]))
+
+
+def test_dW_rows_reject_a_wrong_lse():
+    """The selected rows depend on every token's lse: an lse taken from the
+    top-K ids only, or shifted by a constant, moves them visibly."""
+    H, W, idx, p = _rand_case(6, 5, 30, 4, seed=33)
+    full = kd_oracle(H, W, idx, p)
+    vrows = np.arange(0, 30, 3)
+    ref = full["dW"][vrows]
+    z = H @ W.T
+    zk = np.take_along_axis(z, idx.astype(np.int64), 1)
+    lse_topk = zk.max(1) + np.log(np.exp(zk - zk.max(1, keepdims=True)).sum(1))
+    for bad in (lse_topk, full["lse"] + 0.05, full["lse"][::-1].copy()):
+        got = kd_oracle_dW_rows(H, W, idx, p, bad, vrows)
+        assert np.abs(got - ref).max() > 1e-3 * np.abs(ref).max()
 
 
 # ---------------------------------------------------------------- pin sensitivity
