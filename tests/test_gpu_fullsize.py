@@ -1,80 +1,121 @@
-"""Parity at the workloads' full sizes.
+"""Parity at the workloads' full sizes, for both fused steps (with and without
+the backward recompute).
 
 1. Every head shape (d, V, K) at full size with a few hundred tokens in
    ragged 128-row chunks: every output element against the fp64 oracle.
-2. The benchmark's launch configuration (long-context head, chunk 2048) over
-   two chunks, the second ragged: every element, dW included.
-3. Full sequence lengths (8K, 32K, 128K, 256K tokens): lse, per-row loss and dH
-   on sampled rows (first / last rows of chunks included) against the oracle,
-   which computes each sampled row on its own; the loss equals the sum of the
-   per-row losses; and dW is tied to dH by <W, dW> = <H, dH> (both are
-   sum_tj G_tj z_tj for the same bf16 G), which fails if a chunk's dW is lost,
-   offset or transposed.
+2. The benchmark's launch configuration (long-context head, chunk 2048) and
+   the large-vocabulary head's (d 2880, V 201088, chunk 2048) over two chunks,
+   the second ragged: every element, dW included.  Both run the two-CTA form,
+   so the large-vocabulary case takes the pair-form dW through a 64-column d
+   tail and a 201,088-word vocabulary.
+3. The 3B head at its full 8192 tokens (chunk 1024) and the scaling sweep's
+   first point (4096 tokens, d 4096, chunk 4096): every element of every
+   output against the oracle's full forward and backward.
+4. The long-context workload at its full 32768 tokens: the oracle's forward
+   over every row gives the total loss and every lse and per-row loss; dH is
+   checked on 256 sampled rows (every chunk's first and last row among them)
+   and dW on 256 sampled vocabulary rows, computed from the oracle's own lse
+   of all 32768 rows.
+5. The large-vocabulary head at 131072 tokens and the sweep's 262144-token
+   point, too large for the oracle's full forward here: lse, per-row loss and
+   dH on 256 sampled rows with every chunk's first and last row.
+Cases 3-5 also hold dW to dH through eight seeded projection identities
+<W u v^T, dW> = <dH, H v u^T>, which change when any group of dW rows is lost,
+scaled, offset or transposed.
 """
 import numpy as np
 import pytest
 import torch
 
 from lm_head_top_tma_b300 import api
-from lm_head_top_tma_b300.inputs import get_workload, make_inputs, sweep_workload
-from parity_util import (LROW_ATOL, LSE_ATOL, GRAD_FRAC, assert_close_full, kd_oracle, kd_oracle_rows,
-                         run_fused, to_dev)
+from lm_head_top_tma_b300.inputs import get_workload
+from parity_util import (GRAD_FRAC, LROW_ATOL, LSE_ATOL, assert_close_full,
+                         assert_projection_identities, fused_to_host, full_case, grad_err,
+                         kd_oracle_rows, run_fused, sample_rows, sample_vocab_rows, to_dev)
+from oracle import kd_oracle_dW_rows
 
 pytestmark = pytest.mark.gpu
 
 HEADS = ["head3b", "bigvocab", "sweep4096"]
+STEPS = [pytest.param(True, id="recompute"), pytest.param(False, id="norecompute")]
 
 
+def _step(recompute):
+    return api.fused_step if recompute else api.fused_step_norecompute
+
+
+@pytest.mark.parametrize("recompute", STEPS)
 @pytest.mark.parametrize("name", HEADS)
-def test_full_head_small_T(cuda_device, name):
+def test_full_head_small_T(cuda_device, name, recompute):
+    inp, ref = full_case(name, T=300, oracle="grads")
+    got = run_fused(inp["H"], inp["W"], inp["idx"], inp["p"], 128, recompute=recompute)
+    assert_close_full(got, ref)
+
+
+@pytest.mark.parametrize("recompute", STEPS)
+@pytest.mark.parametrize("name", ["longctx", "bigvocab"])
+def test_two_chunks_pair_form(cuda_device, name, recompute):
     wl = get_workload(name)
-    inp = make_inputs(wl, device=cuda_device, T=300)
-    ref = kd_oracle(inp["H"].cpu(), inp["W"].cpu(), inp["idx"], inp["p"])
-    got = run_fused(inp["H"], inp["W"], inp["idx"], inp["p"], 128)
+    inp, ref = full_case(name, T=wl.chunk + 300, oracle="grads")
+    got = run_fused(inp["H"], inp["W"], inp["idx"], inp["p"], wl.chunk, recompute=recompute)
     assert_close_full(got, ref)
 
 
-def test_bench_launch_configuration_two_chunks(cuda_device):
-    wl = get_workload("longctx")
-    inp = make_inputs(wl, device=cuda_device, T=wl.chunk + 300)
-    ref = kd_oracle(inp["H"].cpu(), inp["W"].cpu(), inp["idx"], inp["p"])
-    got = run_fused(inp["H"], inp["W"], inp["idx"], inp["p"], wl.chunk)
-    assert_close_full(got, ref)
-
-
-def _sample_rows(T, chunk, n=40, seed=0):
-    rng = np.random.default_rng(seed)
-    edges = {0, T - 1}
-    for c0 in range(0, T, chunk):
-        edges.update({c0, min(T - 1, c0 + chunk - 1)})
-    edges = sorted(edges)[:16]
-    extra = rng.choice(T, size=n - len(edges), replace=False)
-    return np.unique(np.concatenate([np.array(edges), extra]))
-
-
-@pytest.mark.parametrize("name", ["head3b", "longctx", "bigvocab", "sweep262144"])
-def test_full_T_sampled(cuda_device, name):
-    wl = sweep_workload(262144) if name == "sweep262144" else get_workload(name)
-    inp = make_inputs(wl, device=cuda_device)
+@pytest.mark.parametrize("recompute", STEPS)
+@pytest.mark.parametrize("name", ["head3b", "sweep4096"])
+def test_full_T_every_element(cuda_device, name, recompute):
+    inp, ref = full_case(name, oracle="grads")
+    wl = inp["workload"]
     H, W = inp["H"], inp["W"]
     idx, p = to_dev(inp["idx"], inp["p"], cuda_device)
-    res = api.fused_step(H, W, idx, p, wl.chunk, loss_rows=True)
+    res = _step(recompute)(H, W, idx, p, wl.chunk, loss_rows=True)
+    assert_projection_identities(H, W, res["dH"], res["dW"])
+    assert_close_full(fused_to_host(res), ref)
+
+
+@pytest.mark.parametrize("recompute", STEPS)
+def test_longctx_full_T(cuda_device, recompute):
+    inp, ref = full_case("longctx", oracle="forward")     # the oracle's forward over all 32768 rows
+    wl = inp["workload"]
+    H, W = inp["H"], inp["W"]
+    idx, p = to_dev(inp["idx"], inp["p"], cuda_device)
+    res = _step(recompute)(H, W, idx, p, wl.chunk, loss_rows=True)
     torch.cuda.synchronize()
-    rows = _sample_rows(wl.T, wl.chunk)
-    ref = kd_oracle_rows(H[torch.as_tensor(rows, device=cuda_device)].cpu(), W.cpu(),
-                         inp["idx"][rows], inp["p"][rows], np.arange(len(rows)))
+    got = {"loss": float(res["loss"].item()), "lse": res["lse"].double().cpu().numpy(),
+           "loss_rows": res["loss_rows"].double().cpu().numpy()}
+    assert_close_full(got, ref, what=("loss", "lse", "loss_rows"))
+    # dH on sampled rows, every chunk edge included
+    rows = sample_rows(wl.T, wl.chunk)
+    sel = torch.as_tensor(rows, device=cuda_device)
+    ref_rows = kd_oracle_rows(H[sel].cpu(), W.cpu(), inp["idx"][rows], inp["p"][rows], np.arange(len(rows)))
+    assert grad_err(res["dH"][sel].double().cpu().numpy(), ref_rows["dH"]) <= GRAD_FRAC
+    # dW on sampled vocabulary rows, from the oracle's own lse of every token
+    vrows = sample_vocab_rows(wl.V, inp["idx"])
+    ref_dW = kd_oracle_dW_rows(H.cpu(), W.cpu(), inp["idx"], inp["p"], ref["lse"], vrows)
+    got_dW = res["dW"][torch.as_tensor(vrows, device=cuda_device)].double().cpu().numpy()
+    assert grad_err(got_dW, ref_dW) <= GRAD_FRAC
+    assert_projection_identities(H, W, res["dH"], res["dW"])
+
+
+@pytest.mark.parametrize("recompute", STEPS)
+@pytest.mark.parametrize("name", ["bigvocab", "sweep262144"])
+def test_full_T_sampled(cuda_device, name, recompute):
+    inp, ref = full_case(name, oracle="rows")
+    wl = inp["workload"]
+    H, W = inp["H"], inp["W"]
+    idx, p = to_dev(inp["idx"], inp["p"], cuda_device)
+    res = _step(recompute)(H, W, idx, p, wl.chunk, loss_rows=True)
+    torch.cuda.synchronize()
+    rows = ref["rows"]
+    assert len(rows) >= 256 and {0, wl.chunk - 1, wl.chunk, wl.T - 1} <= set(rows.tolist())
+    sel = torch.as_tensor(rows, device=cuda_device)
     lse = res["lse"].double().cpu().numpy()
     lrows = res["loss_rows"].double().cpu().numpy()
-    dH_rows = res["dH"][torch.as_tensor(rows, device=cuda_device)].double().cpu().numpy()
     assert np.abs(lse[rows] - ref["lse"]).max() <= LSE_ATOL
     assert np.abs(lrows[rows] - ref["loss_rows"]).max() <= LROW_ATOL
-    scale = np.abs(ref["dH"]).max()
-    assert np.abs(dH_rows - ref["dH"]).max() <= GRAD_FRAC * scale
+    assert grad_err(res["dH"][sel].double().cpu().numpy(), ref["dH"]) <= GRAD_FRAC
     # the loss is the fixed-order fp64 sum of the per-row losses (rounded to fp32 once)
     loss = res["loss"].item()
     assert abs(loss - lrows.sum()) <= 1e-5 * abs(lrows.sum()) + 1e-3
-    # <W, dW> == <H, dH>
-    lhs = torch.sum(W.double() * res["dW"].double()).item()
-    rhs = torch.sum(H.double() * res["dH"].double()).item()
-    assert abs(lhs - rhs) <= 1e-3 * max(abs(lhs), abs(rhs)), (lhs, rhs)
+    assert_projection_identities(H, W, res["dH"], res["dW"])
     assert torch.isfinite(res["dW"]).all()
