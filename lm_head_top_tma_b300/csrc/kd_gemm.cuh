@@ -182,8 +182,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + NST * Cfg::STAGE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + staging_bytes(EPI));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NST + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NST + 7);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // CTA rank within the pair (0 = leader: issues the MMAs, owns D rows 0-127 of each tile)
@@ -191,10 +192,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const bool leader = rank == 0;
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
-  // barrier map: full[s], empty[s], tmem_full[2], tmem_empty[2], drain
+  // barrier map: full[s], empty[s], tmem_full[2], tmem_empty[2], drain, and for a
+  // pair's wind-down: peer_done (leader: the peer reported its loads), drained
+  // (peer: the leader saw every load land)
   const uint32_t full0 = bar0, empty0 = bar0 + 8u * NST;
   const uint32_t tfull0 = bar0 + 16u * NST, tempty0 = tfull0 + 16u;
   const uint32_t drain_bar = tempty0 + 16u;
+  const uint32_t peer_done_bar = drain_bar + 8u, drained_bar = drain_bar + 16u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -206,7 +210,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(tempty0 + 8u * a, EPI_WARPS * Cfg::NCTA);  // both CTAs' epilogue warps release
     }
     mbar_init(drain_bar, 1);
+    mbar_init(peer_done_bar, 1);
+    mbar_init(drained_bar, 1);
     *abort_flag = 0;
+    *peer_issued = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -233,7 +240,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_par = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;  // k-blocks whose loads this CTA issued; k-block n uses stage n % NST
       bool ok = true;
       for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
         int m, n, s;
@@ -255,11 +263,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint32_t a_dst = smem_base + stage * Cfg::STAGE;
           const uint32_t b_dst = a_dst + A_STAGE_BYTES;
           if (!P.debug_withhold_loads) {
-            if (leader) {
-              mbar_arrive_expect_tx(fb_local, Cfg::NCTA * Cfg::STAGE);
-              armed |= 1u << stage;
-              armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-            }
+            if (leader) mbar_arrive_expect_tx(fb_local, Cfg::NCTA * Cfg::STAGE);
             if (!A_MN) {
               load_tile<PAIR>(a_dst, &tmA, P.a_k0 + kb * BK, a_row, fb);
             } else {
@@ -274,6 +278,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int j = 0; j < Cfg::B_ROWS / 64; ++j)
                 load_tile<PAIR>(b_dst + j * 8192, &tmB, b_row + j * 64, P.b_k0 + kb * BK, fb);
             }
+            ++issued;
           }
           if (++stage == NST) {
             stage = 0;
@@ -281,14 +286,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
-      if (!ok) {  // let copies already in flight land before the CTA exits
-        for (int s2 = 0; s2 < NST; ++s2)
-          if ((armed >> s2) & 1u) mbar_wait_quiet(full0 + 8u * s2, (armed_par >> s2) & 1u, P.wait_limit_ns);
-        if constexpr (PAIR) {  // the peer cannot observe its own loads: give them time to land
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 200000ull) {
+      // Wind-down: no copy may still be in flight when the CTA (or pair) exits.
+      // Every k-block older than the last NST was consumed by the MMA (its
+      // stage was reused), so only the last NST can be outstanding, and they
+      // are outstanding only after an abort.  A pair's loads all signal the
+      // leader's barriers, which the peer cannot wait on: the peer reports how
+      // many k-blocks it loaded, the leader balances the barriers of k-blocks
+      // that only one CTA loaded (arming those only the peer loaded, and
+      // completing the peer's share of those only the leader loaded), waits
+      // for them to land, and then tells the peer.  Every wait is bounded.
+      if constexpr (PAIR) {
+        if (!leader) {
+          st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_issued)), 0), issued);
+          mbar_arrive_cluster(mapa_shared(peer_done_bar, 0));
+          mbar_wait_quiet(drained_bar, 0, P.wait_limit_ns);
+        } else {
+          // the peer reaches this point within one wait limit of the leader
+          const uint32_t np = mbar_wait_quiet_cluster(peer_done_bar, 0, 2 * P.wait_limit_ns) ? *peer_issued
+                                                                                             : issued;
+          const uint32_t hi = max(issued, np);
+          const uint32_t lo = hi > static_cast<uint32_t>(NST) ? hi - NST : 0u;
+          for (uint32_t q = lo; q < hi; ++q) {
+            const uint32_t fb = full0 + 8u * (q % NST);
+            if (q >= issued) mbar_arrive_expect_tx(fb, Cfg::STAGE);  // only the peer's share was loaded
+            else if (q >= np) mbar_complete_tx(fb, Cfg::STAGE);      // the peer's share never will be
           }
+          for (uint32_t q = lo; q < hi; ++q)
+            mbar_wait_quiet(full0 + 8u * (q % NST), (q / NST) & 1u, P.wait_limit_ns);
+          mbar_arrive_cluster(mapa_shared(drained_bar, 1));
         }
+      } else if (!ok) {
+        const uint32_t lo = issued > static_cast<uint32_t>(NST) ? issued - NST : 0u;
+        for (uint32_t q = lo; q < issued; ++q)
+          mbar_wait_quiet(full0 + 8u * (q % NST), (q / NST) & 1u, P.wait_limit_ns);
       }
     }
   } else if (warp == 1) {
