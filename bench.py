@@ -42,9 +42,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); peak bytes vs T"
 
-# DRAM traffic per launch of the kernels that can dominate the step, from ncu
-# captures (profiles/gemm_traffic_longctx_chunk2048.md); reported only while the
-# kernel sources still hash to what was captured.  gemm_dw: one launch per group
+# DRAM traffic per launch of the kernels that can dominate the step, carried
+# over from one-pass ncu captures (dram__bytes_read.sum + dram__bytes_write.sum)
+# of the same command at T 8192; reported only while the kernel sources still
+# hash to what was captured.  gemm_dw: one launch per group
 # of two 2048-row chunks, the first group of a step stores dW ("first"), the
 # others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
 # chunk's forward.
@@ -53,6 +54,8 @@ TRAFFIC = {"workload": "longctx", "src_sha": "4686b7befbdcac5d", "kinds": {
     "logits_gf": {"first": 916718592 + 522833920,
                   "rest": (880588288 + 523105024 + 897105152 + 522820864) // 2},
 }}
+# sequence lengths of the peak-bytes-versus-T series (the output-head-only benchmark's range)
+PEAK_T = (4096, 8192, 16384, 32768, 65536, 131072, 262144)
 KERNEL_SOURCES = ["lm_head_top_tma_b300/csrc/kd_gemm.cuh", "lm_head_top_tma_b300/csrc/kd_ptx.cuh",
                   "lm_head_top_tma_b300/csrc/kdtopk.cu"]
 
@@ -302,9 +305,7 @@ def run_kdtopk(args):
     N.check(api.device_status(work.buf, dev), "warm-up")
     torch.cuda.synchronize(dev)
 
-    # ---- device-resident timed region
-    api.profile_enable(True)
-    api.profile_read(reset=True)
+    # ---- device-resident timed region (no per-kernel events inside it)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -318,13 +319,27 @@ def run_kdtopk(args):
     torch.cuda.synchronize(dev)
     barrier(ws)
     clk = clocks.stop()
-    prof = api.profile_read(reset=True)
-    api.profile_enable(False)
     N.check(api.device_status(work.buf, dev), "timed steps")
     ms = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms, ws)
     tokens_per_s = ws * T / (ms / 1e3)
     peak_bytes = torch.cuda.max_memory_allocated(dev)  # inputs + outputs + workspace of the step
+
+    # ---- the same K steps again with a CUDA event pair around every launch, on the
+    # launching stream: the per-kernel breakdown, the launch count and the dominant
+    # kernel's roofline come from this second loop
+    api.profile_enable(True)
+    api.profile_read(reset=True)
+    ep0, ep1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ep0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ep1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = api.profile_read(reset=True)
+    api.profile_enable(False)
+    N.check(api.device_status(work.buf, dev), "profiled steps")
+    ms_profiled = ep0.elapsed_time(ep1) / args.steps
 
     # ---- end to end: every step's inputs copied in from pinned host memory and its loss
     # read back.  The copies run on a side stream into two device buffers, so step k+1's
@@ -440,6 +455,19 @@ def run_kdtopk(args):
             "tflops_8TVd": ws * 8.0 * T * V * d / (ms_fb / 1e3) / 1e12}
         del dW_sep
 
+        # ---- the teacher-cache builder (the offline step that produces the cache)
+        variants["topk_cache_build"] = time_topk_cache(dev, 32768, 128256, 100, args.steps, args.warmup)
+
+    # ---- peak bytes versus T on the benchmark head (one warm-up and one timed step per T)
+    peak_vs_T = None
+    ws_nbytes = work.nbytes
+    if not args.no_variants and not args.no_peak_sweep:
+        del out, work
+        torch.cuda.empty_cache()
+        peak_vs_T = {"head": {"d": d, "V": V, "K": K, "chunk": C},
+                     "inputs": f"H, W drawn as the {wl.name} workload's; its teacher cache repeated to T rows",
+                     "points": peak_bytes_vs_T(dev, wl, inp["idx"], inp["p"], PEAK_T)}
+
     flops_8 = 8.0 * T * V * d
     flops_6 = 6.0 * T * V * d
     peaks = load_peaks()
@@ -466,9 +494,16 @@ def run_kdtopk(args):
         traffic = (tk["first"] + (n_launch - 1) * tk["rest"]) / n_launch
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sustained"],
                 "unit": "TFLOP/s", "frac": (achieved / peaks["bf16_sustained"]) if achieved else None,
-                "traffic": traffic, "peak_kind": f"bf16 sustained ({peaks['source']})",
+                "traffic": traffic,
+                "traffic_source": ("carried over from a one-pass ncu capture (DRAM read + write bytes per launch) "
+                                   f"of the same kernel sources (hash {TRAFFIC['src_sha']}), not measured in this run"
+                                   if traffic is not None else "no capture of the current kernel sources"),
+                "peak_kind": f"bf16 sustained ({peaks['source']})",
                 "flops_per_launch": per_launch_flops,
                 "frac_of_burst_peak": (achieved / peaks["bf16"]) if achieved else None,
+                "timing": "CUDA events around each launch on the launching stream, in a second loop of the same "
+                          f"{args.steps} steps after the unprofiled headline loop ({ms_profiled:.2f} ms/step with "
+                          "the events)",
                 "per_kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
                 "launches_per_step": {k: v[1] // args.steps for k, v in prof.items() if v[1]}}
 
@@ -490,13 +525,14 @@ def run_kdtopk(args):
             "frac_of_bf16_peak": {"burst": ws * flops_8 / (ms / 1e3) / 1e12 / ws / peaks["bf16"],
                                   "sustained": ws * flops_8 / (ms / 1e3) / 1e12 / ws / peaks["bf16_sustained"],
                                   "source": peaks["source"]},
-            "workspace_bytes": work.nbytes, "peak_bytes": peak_bytes,
+            "workspace_bytes": ws_nbytes, "peak_bytes": peak_bytes,
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": ws * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": 4},
             "gpu_launches": launches,
             "clocks": clk,
             "variants": variants,
+            "peak_bytes_vs_T": peak_vs_T,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -554,52 +590,108 @@ def run_sweep(args):
     return 0
 
 
-def run_topk_cache(args):
-    """Teacher-cache builder: top-K ids and probabilities of every row of
-    synthetic teacher logits Z [T, V] (bf16, or fp32 with --logits-dtype fp32),
-    one JSON line.  HBM-bound: the algorithmic bytes are one read of Z plus the
-    cache written (idx, p, lse)."""
+def time_topk_cache(dev, T, V, K, steps, warmup, dtype="bf16"):
+    """Teacher-cache builder on synthetic teacher logits Z [T, V] (bf16 or fp32):
+    CUDA-event time of `steps` launches on the launching stream, and the HBM
+    roofline.  Algorithmic bytes per launch: one read of Z plus the cache
+    written (idx, p) and lse."""
     import torch
 
     from lm_head_top_tma_b300 import api
     from lm_head_top_tma_b300.inputs import make_teacher_logits
 
-    dev = torch.device("cuda:0")
-    torch.cuda.set_device(dev)
-    T, V, K = args.T or 32768, 128256, 100
-    Z = make_teacher_logits(T, V, seed=7, device=dev, dtype=args.logits_dtype)
-    for _ in range(max(3, args.warmup)):
-        api.topk_cache_build(Z, K)
+    Z = make_teacher_logits(T, V, seed=7, device=dev, dtype=dtype)
+    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    p = torch.empty(T, K, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    for _ in range(max(3, warmup)):
+        api.topk_cache_build(Z, K, out=(idx, p, lse))
     torch.cuda.synchronize(dev)
-    api.profile_enable(True)
-    api.profile_read(reset=True)
-    clocks = ClockSampler(0)
+    clocks = ClockSampler(dev.index or 0)
     clocks.start()
     time.sleep(0.3)
     stream = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        api.topk_cache_build(Z, K)
+    for _ in range(steps):
+        api.topk_cache_build(Z, K, out=(idx, p, lse))
     e1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    prof = api.profile_read(reset=True)
-    api.profile_enable(False)
-    ms = e0.elapsed_time(e1) / args.steps
-    kern_ms, kern_n = prof["other"]
+    ms = e0.elapsed_time(e1) / steps
     bytes_alg = T * V * Z.element_size() + T * K * 8 + T * 4
     peaks = load_peaks()
-    achieved = bytes_alg / (kern_ms / kern_n / 1e3) / 1e9
+    achieved = bytes_alg / (ms / 1e3) / 1e9
+    del Z, idx, p, lse
+    torch.cuda.empty_cache()
+    return {"value": T / (ms / 1e3), "unit": "rows/s", "ms_per_launch": ms, "launches": steps,
+            "config": {"workload": "teacher_logits", "T": T, "V": V, "K": K, "logits_dtype": dtype,
+                       "l2": "logits larger than L2, no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm"], "traffic": None, "bytes_per_launch": bytes_alg,
+                         "peak_kind": f"HBM copy ({peaks['source']})"},
+            "clocks": clk}
+
+
+def run_topk_cache(args):
+    """Teacher-cache builder: top-K ids and probabilities of every row of
+    synthetic teacher logits Z [T, V] (bf16, or fp32 with --logits-dtype fp32),
+    one JSON line."""
+    import torch
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    r = time_topk_cache(dev, args.T or 32768, 128256, 100, args.steps, args.warmup, args.logits_dtype)
     print(json.dumps({
-        "metric": "teacher top-K cache build rows/s", "value": T / (ms / 1e3), "unit": "rows/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "dtype": args.logits_dtype, "data": "synthetic", "config": {"workload": "teacher_logits", "T": T, "V": V, "K": K,
-                                                          "l2": "logits larger than L2, no flush"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm"], "traffic": None, "bytes_per_launch": bytes_alg},
-        "clocks": clk}), flush=True)
+        "metric": "teacher top-K cache build rows/s", "value": r["value"], "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_launch"], "higher_is_better": True,
+        "dtype": args.logits_dtype, "data": "synthetic", "config": r["config"], "roofline": r["roofline"],
+        "clocks": r["clocks"]}), flush=True)
     return 0
+
+
+def peak_bytes_vs_T(dev, wl, idx_host, p_host, Ts):
+    """Library workspace and device peak of one fused step at each sequence
+    length T on the given head (d, V, K, chunk): H and W drawn as the
+    workload's, the teacher cache the workload's own rows repeated to T rows.
+    One warm-up step, then one step timed with CUDA events.  ``peak_bytes`` is
+    the allocator's peak during the step minus what was allocated before its
+    inputs existed, so it counts exactly the step's inputs, outputs and
+    workspace."""
+    import numpy as np
+    import torch
+
+    from lm_head_top_tma_b300 import _native as N
+    from lm_head_top_tma_b300 import api
+    from lm_head_top_tma_b300.inputs import make_hw
+
+    rows = []
+    for T in Ts:
+        torch.cuda.synchronize(dev)
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        H, W = make_hw(T, wl.d, wl.V, wl.kind, wl.seed, device=dev)
+        reps = -(-T // idx_host.shape[0])
+        idx = torch.as_tensor(np.tile(idx_host, (reps, 1))[:T]).to(dev)
+        p = torch.as_tensor(np.tile(p_host, (reps, 1))[:T]).to(dev)
+        work = api.Workspace(dev)
+        out = {"loss": torch.empty(1, device=dev), "lse": torch.empty(T, device=dev),
+               "dH": torch.empty(T, wl.d, device=dev), "dW": torch.empty(wl.V, wl.d, device=dev)}
+        api.fused_step(H, W, idx, p, wl.chunk, workspace=work, out=out, check=False)
+        N.check(api.device_status(work.buf, dev), f"peak-bytes step at T {T}")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.fused_step(H, W, idx, p, wl.chunk, workspace=work, out=out, check=False)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        N.check(api.device_status(work.buf, dev), f"peak-bytes step at T {T}")
+        ms = e0.elapsed_time(e1)
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        rows.append({"T": T, "workspace_bytes": work.nbytes, "peak_bytes": peak, "ms_per_step": ms,
+                     "tokens_per_s": T / (ms / 1e3), "tflops_8TVd": 8.0 * T * wl.V * wl.d / (ms / 1e3) / 1e12})
+        del H, W, idx, p, out, work
+        torch.cuda.empty_cache()
+    return rows
 
 
 def main():
@@ -612,7 +704,9 @@ def main():
     ap.add_argument("--T", type=int, default=None, help="override the sequence length (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-variants", action="store_true", help="skip the no-recompute fused step timing")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip everything but the fused step (variants, peak bytes versus T)")
+    ap.add_argument("--no-peak-sweep", action="store_true", help="skip the peak-bytes-versus-T series")
     ap.add_argument("--sweep", action="store_true", help="output-head-only T sweep, one line per T")
     ap.add_argument("--topk-cache", action="store_true", help="teacher-cache builder over synthetic logits")
     ap.add_argument("--logits-dtype", default="bf16", choices=["bf16", "fp32"],

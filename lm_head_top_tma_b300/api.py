@@ -186,19 +186,31 @@ def _fused(fn, name, H, W, idx, p, chunk, dloss, dW, accumulate_dW, loss_rows, w
     return res
 
 
-def topk_cache_build(Z, K: int, *, lse: bool = True):
+def topk_cache_build(Z, K: int, *, lse: bool = True, out=None):
     """Teacher cache from logits Z [T,V] (bf16 or fp32, CUDA): ids of the K
     largest logits (largest first, ties by ascending id), their softmax
-    probabilities, and lse.  Returns (idx int32 [T,K], p fp32 [T,K], lse fp32 [T] or None)."""
+    probabilities, and lse.  Returns (idx int32 [T,K], p fp32 [T,K], lse fp32 [T] or None).
+    ``out`` = (idx, p, lse or None) reuses caller-owned output tensors."""
     if not isinstance(Z, torch.Tensor) or not Z.is_cuda or Z.dim() != 2 or not Z.is_contiguous():
         raise ValueError("Z must be a contiguous 2-D CUDA tensor")
     if Z.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("Z must be bf16 or fp32")
     T, V = Z.shape
     dev = Z.device
-    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
-    p = torch.empty(T, K, dtype=torch.float32, device=dev)
-    l = torch.empty(T, dtype=torch.float32, device=dev) if lse else None
+    if out is not None:
+        idx, p, l = out
+        _need(idx, "idx", torch.int32, 2, dev)
+        _need(p, "p", torch.float32, 2, dev)
+        if tuple(idx.shape) != (T, K) or tuple(p.shape) != (T, K):
+            raise ValueError("out idx and p must be [T, K]")
+        if l is not None:
+            _need(l, "lse", torch.float32, 1, dev)
+            if l.shape[0] != T:
+                raise ValueError("out lse must be [T]")
+    else:
+        idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+        p = torch.empty(T, K, dtype=torch.float32, device=dev)
+        l = torch.empty(T, dtype=torch.float32, device=dev) if lse else None
     rc = N.load().kd_topk_cache_build(_ptr(Z), int(Z.dtype == torch.bfloat16), T, V, int(K), _ptr(idx), _ptr(p),
                                       _ptr(l), _stream(dev))
     N.check(rc, "kd_topk_cache_build")
