@@ -43,16 +43,17 @@ sys.path.insert(0, ROOT)
 METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); peak bytes vs T"
 
 # DRAM traffic per launch of the kernels that can dominate the step, carried
-# over from one-pass ncu captures (dram__bytes_read.sum + dram__bytes_write.sum)
-# of the same command at T 8192; reported only while the kernel sources still
-# hash to what was captured.  gemm_dw: one launch per group
+# over from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# same command at T 8192, where every launch does the work of a launch at
+# T 32768; reported only while the kernel sources still hash to what was
+# captured.  gemm_dw: one launch per group
 # of two 2048-row chunks, the first group of a step stores dW ("first"), the
 # others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
 # chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": "4686b7befbdcac5d", "kinds": {
-    "gemm_dw": {"first": 1515243520 + 1545350912, "rest": 2793174528 + 1538373632},
-    "logits_gf": {"first": 916718592 + 522833920,
-                  "rest": (880588288 + 523105024 + 897105152 + 522820864) // 2},
+TRAFFIC = {"workload": "longctx", "src_sha": "3bd9eb916468744c", "kinds": {
+    "gemm_dw": {"first": 1879218688 + 1541118976, "rest": 3159258624 + 1536683520},
+    "logits_gf": {"first": 1091684096 + 522140672,
+                  "rest": (1035396864 + 522573312 + 1077324288 + 522111488) // 2},
 }}
 # sequence lengths of the peak-bytes-versus-T series (the output-head-only benchmark's range)
 PEAK_T = (4096, 8192, 16384, 32768, 65536, 131072, 262144)
@@ -495,7 +496,7 @@ def run_kdtopk(args):
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_sustained"],
                 "unit": "TFLOP/s", "frac": (achieved / peaks["bf16_sustained"]) if achieved else None,
                 "traffic": traffic,
-                "traffic_source": ("carried over from a one-pass ncu capture (DRAM read + write bytes per launch) "
+                "traffic_source": ("carried over from an ncu capture at T 8192 (DRAM read + write bytes per launch) "
                                    f"of the same kernel sources (hash {TRAFFIC['src_sha']}), not measured in this run"
                                    if traffic is not None else "no capture of the current kernel sources"),
                 "peak_kind": f"bf16 sustained ({peaks['source']})",

@@ -123,6 +123,9 @@ struct GemmParams {
   int m_split, a_mn0_2, rows_valid2;
   const int32_t* sidx2;
   const float* sp2;
+  // MN-major operands whose tensor map is the 3-D view {64, K rows, MN / 64}:
+  // the tile's 64-column blocks arrive in one copy instead of one per block
+  int a_mn3d, b_mn3d;
 };
 
 __device__ __forceinline__ void decode_tile(const GemmParams& P, int tile, int& m, int& n, int& s) {
@@ -161,6 +164,21 @@ template <bool PAIR>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
   if constexpr (PAIR) tma_load_2d_pair(dst, tm, x, y, bar);
   else tma_load_2d(dst, tm, x, y, bar);
+}
+
+// An MN-major tile of `cols` (128 or 256) columns starting at column mn (a
+// multiple of 64) and 64 k-rows starting at k: one 3-D copy when the map is
+// the 3-D view, else one 2-D copy per 64-column block (8 KB apart in shared
+// memory, the layout the 3-D copy produces too).
+template <bool PAIR>
+__device__ __forceinline__ void load_tile_mn(uint32_t dst, const CUtensorMap* tm, bool view3d, int mn, int k, int cols,
+                                             uint32_t bar) {
+  if (view3d) {
+    if constexpr (PAIR) tma_load_3d_pair(dst, tm, 0, k, mn >> 6, bar);
+    else tma_load_3d(dst, tm, 0, k, mn >> 6, bar);
+  } else {
+    for (int j = 0; j < cols / 64; ++j) load_tile<PAIR>(dst + j * 8192, tm, mn + j * 64, k, bar);
+  }
 }
 
 // MMA completion -> mbarrier at offset `bar`: this CTA's (single form) or both
@@ -264,20 +282,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint32_t b_dst = a_dst + A_STAGE_BYTES;
           if (!P.debug_withhold_loads) {
             if (leader) mbar_arrive_expect_tx(fb_local, Cfg::NCTA * Cfg::STAGE);
-            if (!A_MN) {
-              load_tile<PAIR>(a_dst, &tmA, P.a_k0 + kb * BK, a_row, fb);
-            } else {
-#pragma unroll
-              for (int j = 0; j < BM / 64; ++j)
-                load_tile<PAIR>(a_dst + j * 8192, &tmA, a_row + j * 64, P.a_k0 + kb * BK, fb);
-            }
-            if (!B_MN) {
-              load_tile<PAIR>(b_dst, &tmB, P.b_k0 + kb * BK, b_row, fb);
-            } else {
-#pragma unroll
-              for (int j = 0; j < Cfg::B_ROWS / 64; ++j)
-                load_tile<PAIR>(b_dst + j * 8192, &tmB, b_row + j * 64, P.b_k0 + kb * BK, fb);
-            }
+            if (!A_MN) load_tile<PAIR>(a_dst, &tmA, P.a_k0 + kb * BK, a_row, fb);
+            else load_tile_mn<PAIR>(a_dst, &tmA, P.a_mn3d != 0, a_row, P.a_k0 + kb * BK, BM, fb);
+            if (!B_MN) load_tile<PAIR>(b_dst, &tmB, P.b_k0 + kb * BK, b_row, fb);
+            else load_tile_mn<PAIR>(b_dst, &tmB, P.b_mn3d != 0, b_row, P.b_k0 + kb * BK, Cfg::B_ROWS, fb);
             ++issued;
           }
           if (++stage == NST) {

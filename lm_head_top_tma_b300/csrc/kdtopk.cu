@@ -73,6 +73,37 @@ bool tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view {64, rows, mn / 64} of a row-major bf16 matrix [rows, mn] read as an
+// MN-major GEMM operand (mn the contiguous index): one box of {64, BK, nblk}
+// is nblk consecutive 64-column blocks of BK rows, laid out in shared memory
+// exactly as nblk 2-D boxes of {64, BK}.  Only when mn % 64 == 0, so that the
+// view never reaches past a row's last element; out-of-range rows and blocks
+// are zero-filled as in the 2-D map.
+bool tmap_bf16_mn3d(CUtensorMap* tm, const void* base, uint64_t mn, uint64_t rows, uint64_t row_bytes,
+                    uint32_t nblk) {
+  auto enc = encode_fn();
+  if (!enc || mn % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, mn / 64};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BK), nblk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// An MN-major operand's map: the 3-D view when mn allows it (*view3d = 1),
+// else the 2-D map with 64-column boxes.
+bool tmap_bf16_mn(CUtensorMap* tm, int* view3d, const void* base, uint64_t mn, uint64_t rows, uint64_t row_bytes,
+                  uint32_t tile_cols) {
+  *view3d = 0;
+  if (mn % 64 == 0 && tmap_bf16_mn3d(tm, base, mn, rows, row_bytes, tile_cols / 64)) {
+    *view3d = 1;
+    return true;
+  }
+  return tmap_bf16(tm, base, mn, rows, row_bytes, 64, BK);
+}
+
 // 2-D fp32 tensor map for the GEMM outputs: 32-column x 128-row boxes, 128-byte swizzle.
 bool tmap_f32_out(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes) {
   auto enc = encode_fn();
@@ -370,6 +401,7 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
 
   // TMA descriptors (all bf16, 128-byte swizzle, 64-element inner boxes)
   CUtensorMap tmH_k, tmW_k, tmG_k, tmW_mn, tmG_mn, tmH_mn, tmDhp, tmDW;
+  int w_mn3d = 0, g_mn3d = 0, h_mn3d = 0;  // MN-major maps that are 3-D views
   const uint64_t hrow = uint64_t(d) * 2;
   const bool pr = pl.pair;
   // K-major B (W in the logits GEMMs): each CTA of a pair stages half of the 256 columns
@@ -377,9 +409,9 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   if (mode & MODE_BWD) {
     const uint64_t grows = uint64_t(pl.dw_group) * pl.Cpad;  // G rows held in the workspace
     ok = ok && tmap_bf16(&tmG_k, G, V, grows, uint64_t(pl.ldg) * 2, BK, BM) &&
-         tmap_bf16(&tmW_mn, W, d, V, hrow, 64, BK) &&
-         tmap_bf16(&tmG_mn, G, V, grows, uint64_t(pl.ldg) * 2, 64, BK) &&
-         tmap_bf16(&tmH_mn, H, d, T, hrow, 64, BK) &&
+         tmap_bf16_mn(&tmW_mn, &w_mn3d, W, d, V, hrow, pr ? BN / 2 : BN) &&
+         tmap_bf16_mn(&tmG_mn, &g_mn3d, G, V, grows, uint64_t(pl.ldg) * 2, BM) &&
+         tmap_bf16_mn(&tmH_mn, &h_mn3d, H, d, T, hrow, pr ? BN / 2 : BN) &&
          tmap_f32_out(&tmDhp, dhp, d, uint64_t(pl.S) * pl.Cpad, uint64_t(d) * 4) &&
          tmap_f32_out(&tmDW, dW, d, V, uint64_t(d) * 4);
   }
@@ -496,6 +528,7 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
     Q.kb_per_split = pl.kbps_dh;
     Q.split_rows = pl.Cpad;
     Q.a_mn0 = gslot * pl.Cpad;
+    Q.b_mn3d = w_mn3d;
     if (!check(launch_gemm_any<EPI_F32, false, true>(pr, KD_K_GEMM_DH, tmG_k, tmW_mn, tmDhp, Q, sms, st)))
       return false;
     {
@@ -519,6 +552,8 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       R.b_k0 = static_cast<int>(int64_t(first) * pl.C);
       R.reduce_add = (first == 0 && !accumulate) ? 0 : 1;
       R.scale = dloss;
+      R.a_mn3d = g_mn3d;
+      R.b_mn3d = h_mn3d;
       if (!check(launch_gemm_any<EPI_F32, true, true>(pr, KD_K_GEMM_DW, tmG_mn, tmH_mn, tmDW, R, sms, st)))
         return false;
     }
@@ -684,9 +719,11 @@ kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = static_cast<int*>(workspace);
   CUtensorMap ta, tb;
-  bool ok = a_mn ? tmap_bf16(&ta, A, M, K, uint64_t(lda) * 2, 64, BK) : tmap_bf16(&ta, A, K, M, uint64_t(lda) * 2, BK, BM);
+  int a3 = 0, b3 = 0;
   const bool pr = cta_pair != 0;
-  ok = ok && (b_mn ? tmap_bf16(&tb, B, N, K, uint64_t(ldb) * 2, 64, BK)
+  bool ok = a_mn ? tmap_bf16_mn(&ta, &a3, A, M, K, uint64_t(lda) * 2, BM)
+                 : tmap_bf16(&ta, A, K, M, uint64_t(lda) * 2, BK, BM);
+  ok = ok && (b_mn ? tmap_bf16_mn(&tb, &b3, B, N, K, uint64_t(ldb) * 2, pr ? BN / 2 : BN)
                    : tmap_bf16(&tb, B, K, N, uint64_t(ldb) * 2, BK, pr ? BN / 2 : BN));
   CUtensorMap td;
   ok = ok && tmap_f32_out(&td, D, N, M, uint64_t(ldd) * 4);
@@ -696,6 +733,8 @@ kd_status kd_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int
   P.num_m = static_cast<int>(ceil_div(M, pr ? 2 * BM : BM));
   P.num_n = static_cast<int>(ceil_div(N, BN));
   P.kb_total = P.kb_per_split = static_cast<int>(ceil_div(K, BK));
+  P.a_mn3d = a3;
+  P.b_mn3d = b3;
   const int sms = current_sm_count();
   cudaError_t e;
   if (!a_mn && !b_mn) e = launch_gemm_any<EPI_F32, false, false>(pr, KD_K_OTHER, ta, tb, td, P, sms, st);

@@ -11,7 +11,7 @@ from lm_head_top_tma_b300 import api
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(128, 256, 64), (256, 512, 128), (296, 520, 200), (384, 512, 2560), (1024, 768, 3072)]
+SHAPES = [(128, 256, 64), (256, 512, 128), (296, 520, 200), (320, 448, 192), (384, 512, 2560), (1024, 768, 3072)]
 
 
 @pytest.mark.parametrize("pair", [0, 1])
