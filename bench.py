@@ -458,6 +458,8 @@ def run_kdtopk(args):
 
         # ---- the teacher-cache builder (the offline step that produces the cache)
         variants["topk_cache_build"] = time_topk_cache(dev, 32768, 128256, 100, args.steps, args.warmup)
+        variants["topk_cache_build_fp32"] = time_topk_cache(dev, 32768, 128256, 100, args.steps, args.warmup,
+                                                            dtype="fp32")
 
     # ---- peak bytes versus T on the benchmark head (one warm-up and one timed step per T)
     peak_vs_T = None

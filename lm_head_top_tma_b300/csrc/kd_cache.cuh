@@ -8,9 +8,12 @@
 //
 // One block of 512 threads per row (grid-stride over rows, two blocks per
 // SM); each row is read from HBM once, with 16-byte loads, several in flight
-// per thread, after an L2 prefetch of the whole row (its first 64 KB already
-// prefetched while the block selected its previous row, so that HBM keeps
-// streaming through the selection; more than that crowds L2):
+// per thread, after an L2 prefetch of the row.  A row of up to 256 KB is
+// requested whole when its pass 1 starts; a longer row through a window that
+// keeps the next 128 KB ahead of pass 1 requested, so that the rows two
+// blocks per SM hold in L2 stay well inside it.  Either way the first 64 KB
+// of the block's next row is requested while the block selects this one, so
+// that HBM keeps streaming through the selection (more than that crowds L2):
 //   pass 1  per-slot maximum (1024 slots: two per thread, every element in
 //           exactly one), an online (max, sum of 2^x) for lse, and the maximum
 //           of every 16-byte group, kept in shared memory (as bf16, rounded up
@@ -55,6 +58,9 @@ constexpr int CACHE_CAP = 4096;                 // candidates kept in shared mem
 constexpr int CACHE_UNROLL = 4;                 // 16-byte loads in flight per thread
 constexpr int CACHE_GMAX = 32768;               // 16-byte group maxima kept in shared memory
 constexpr int CACHE_GLIST = 1024;               // groups listed for the re-read of pass 2
+constexpr int64_t CACHE_WHOLE_ROW = 262144;     // rows up to this many bytes are prefetched whole
+constexpr int64_t CACHE_PF_WINDOW = 131072;     // bytes kept requested ahead of pass 1 in longer rows
+constexpr int64_t CACHE_PF_HEAD = 65536;        // bytes of the next row requested during selection
 
 // dynamic shared memory of kd_topk_cache_kernel: the candidate list, and the
 // group maxima when rows are read 16 bytes at a time
@@ -337,12 +343,28 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
   const int warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 256; i += CACHE_THREADS) hist[i] = 0;
 
+  const int64_t row_bytes = static_cast<int64_t>(V) * sizeof(TL);
+  const bool windowed = VEC && row_bytes > CACHE_WHOLE_ROW;
+  // thread 0: bytes of the current row already requested into L2, and of the
+  // block's next row (its head, requested during this row's selection)
+  int64_t req = 0, req_next = 0;
+  auto request_upto = [&](const TL* rz, int64_t upto) {  // 16-byte multiples, within the row
+    upto = min(upto, row_bytes);
+    if (upto > req) {
+      prefetch_l2_bulk(reinterpret_cast<const char*>(rz) + req, upto - req);
+      req = upto;
+    }
+  };
   for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
     const RV rv{Z + row * static_cast<int64_t>(V), V};
     const int ng = rv.groups();
     const bool screen = VEC && ng <= CACHE_GMAX;  // group maxima fit in shared memory
     if constexpr (VEC) {
-      if (tid == 0) prefetch_l2_bulk(rv.z, static_cast<int64_t>(V) * sizeof(TL));
+      if (tid == 0) {
+        req = req_next;
+        req_next = 0;
+        request_upto(rv.z, windowed ? CACHE_PF_WINDOW : row_bytes);
+      }
     }
     // ---------------- pass 1: slot maxima, online softmax normaliser, group maxima
     float fslot0 = -INFINITY, fslot1 = -INFINITY;  // two disjoint element sets per thread
@@ -350,6 +372,9 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
     int it = 0;  // the slot of an iteration alternates
     for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL, ++it) {
       float& slot = (it & 1) ? fslot1 : fslot0;
+      // keep the window ahead of what this iteration reads (16 bytes per group)
+      if (windowed && tid == 0)
+        request_upto(rv.z, static_cast<int64_t>(it + 1) * CACHE_THREADS * CACHE_UNROLL * 16 + CACHE_PF_WINDOW);
       if (g0 + (CACHE_UNROLL - 1) * CACHE_THREADS < ng) {
         typename RV::Raw x[CACHE_UNROLL];
         float gm[CACHE_UNROLL];
@@ -410,9 +435,10 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
     const uint32_t theta = prefix;
     if constexpr (VEC) {
       // the head of the block's next row into L2 while this row's selection runs
-      if (tid == 0 && row + gridDim.x < T)
-        prefetch_l2_bulk(rv.z + static_cast<int64_t>(gridDim.x) * V,
-                         min(static_cast<int64_t>(V) * static_cast<int64_t>(sizeof(TL)), int64_t(65536)));
+      if (tid == 0 && row + gridDim.x < T) {
+        req_next = min(row_bytes, CACHE_PF_HEAD);
+        prefetch_l2_bulk(rv.z + static_cast<int64_t>(gridDim.x) * V, req_next);
+      }
     }
 
     // ---------------- pass 2: every element with key >= theta, i.e. value >= theta's value
