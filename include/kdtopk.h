@@ -175,7 +175,9 @@ KD_API kd_status kd_topk_kl_fused_step_norecompute(const void* H, const void* W,
  *     201,088-word vocabulary does not).
  *   - The first call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
+ *     before any stream capture on the device.  The address is kept for the
+ *     life of the process: cudaDeviceReset unloads the array with the
+ *     library's device code, so do not use this entry point across a reset.
  *   - Every call on a device shares the one array and finds the previous
  *     call's contents in it; each call re-initialises what it needs.  Calls
  *     that could overlap on the GPU (other streams, other host threads) race
