@@ -43,17 +43,17 @@ sys.path.insert(0, ROOT)
 METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); peak bytes vs T"
 
 # DRAM traffic per launch of the kernels that can dominate the step, carried
-# over from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# same command at T 8192, where every launch does the work of a launch at
-# T 32768; reported only while the kernel sources still hash to what was
-# captured.  gemm_dw: one launch per group
-# of two 2048-row chunks, the first group of a step stores dW ("first"), the
-# others reduce-add into it ("rest").  logits_gf: one chunk's G with the next
-# chunk's forward.
+# over from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum), one
+# kernel and at most three launches per capture, of the same command at
+# T 8192, where every launch does the work of a launch at T 32768; reported
+# only while the kernel sources still hash to what was captured.  gemm_dw: one
+# launch per group of two 2048-row chunks, the first group of a step stores dW
+# ("first"), the others reduce-add into it ("rest").  logits_gf: one chunk's G
+# with the next chunk's forward.
 TRAFFIC = {"workload": "longctx", "src_sha": "3bd9eb916468744c", "kinds": {
-    "gemm_dw": {"first": 1879218688 + 1541118976, "rest": 3159258624 + 1536683520},
-    "logits_gf": {"first": 1091684096 + 522140672,
-                  "rest": (1035396864 + 522573312 + 1077324288 + 522111488) // 2},
+    "gemm_dw": {"first": 1346497792 + 1544325376, "rest": 2748394752 + 1535060480},
+    "logits_gf": {"first": 905059072 + 524794624,
+                  "rest": (924568064 + 523076864 + 920643840 + 522863104) // 2},
 }}
 # sequence lengths of the peak-bytes-versus-T series (the output-head-only benchmark's range)
 PEAK_T = (4096, 8192, 16384, 32768, 65536, 131072, 262144)
