@@ -187,8 +187,9 @@ def max_over_ranks(x: float, ws: int) -> float:
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def oracle_tokens_per_s(H_cpu, W_cpu, idx, p, target_s: float, rows0: int = 32):
-    """Time the fp64 oracle (forward + backward incl. dW) on a bounded row sample."""
+def oracle_tokens_per_s(H_cpu, W_cpu, idx, p, target_s: float, rows0: int = 128):
+    """Time the fp64 oracle (forward + backward incl. dW) on a bounded row sample,
+    sized from a first run on `rows0` rows to take about `target_s` seconds."""
     import numpy as np
     from oracle import kd_oracle
 
@@ -199,7 +200,7 @@ def oracle_tokens_per_s(H_cpu, W_cpu, idx, p, target_s: float, rows0: int = 32):
     kd_oracle(H_cpu[:n], Wd, idx[:n], p[:n])
     dt = time.perf_counter() - t0
     rows = int(min(T, max(n, n * target_s / max(dt, 1e-6))))
-    rows = max(n, (rows // 32) * 32)
+    rows = max(n, (rows // 64) * 64)
     t0 = time.perf_counter()
     kd_oracle(H_cpu[:rows], Wd, idx[:rows], p[:rows])
     dt = time.perf_counter() - t0
