@@ -706,7 +706,7 @@ def main():
     ap.add_argument("--impl", default="kdtopk", choices=["kdtopk", "reference"])
     ap.add_argument("--workload", default="longctx")
     ap.add_argument("--T", type=int, default=None, help="override the sequence length (profiling runs)")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=25.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip everything but the fused step (variants, peak bytes versus T)")
