@@ -23,6 +23,8 @@ Cases 3-5 also hold dW to dH through eight seeded projection identities
 <W u v^T, dW> = <dH, H v u^T>, which change when any group of dW rows is lost,
 scaled, offset or transposed.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -119,3 +121,29 @@ def test_full_T_sampled(cuda_device, name, recompute):
     assert abs(loss - lrows.sum()) <= 1e-5 * abs(lrows.sum()) + 1e-3
     assert_projection_identities(H, W, res["dH"], res["dW"])
     assert torch.isfinite(res["dW"]).all()
+
+
+@pytest.mark.skipif(os.environ.get("KD_FULL_ORACLE") != "1",
+                    reason="the oracle's forward over every row takes 5-8 minutes here; set KD_FULL_ORACLE=1")
+@pytest.mark.parametrize("name", ["bigvocab", "sweep262144"])
+def test_full_T_against_the_oracle_forward(cuda_device, name):
+    """The largest workloads at full length against the oracle's forward over
+    every row: total loss, every lse and per-row loss, and dW on 256 sampled
+    vocabulary rows computed from the oracle's own lse."""
+    inp, ref = full_case(name, oracle="forward")
+    wl = inp["workload"]
+    H, W = inp["H"], inp["W"]
+    idx, p = to_dev(inp["idx"], inp["p"], cuda_device)
+    res = api.fused_step(H, W, idx, p, wl.chunk, loss_rows=True)
+    torch.cuda.synchronize()
+    got = {"loss": float(res["loss"].item()), "lse": res["lse"].double().cpu().numpy(),
+           "loss_rows": res["loss_rows"].double().cpu().numpy()}
+    rel = abs(got["loss"] - ref["loss"]) / abs(ref["loss"])
+    print(f"\n{name}: loss rel err {rel:.3e}, lse max err {np.abs(got['lse'] - ref['lse']).max():.3e}, "
+          f"per-row loss max err {np.abs(got['loss_rows'] - ref['loss_rows']).max():.3e}")
+    assert_close_full(got, ref, what=("loss", "lse", "loss_rows"))
+    vrows = sample_vocab_rows(wl.V, inp["idx"])
+    ref_dW = kd_oracle_dW_rows(H.cpu(), W.cpu(), inp["idx"], inp["p"], ref["lse"], vrows)
+    got_dW = res["dW"][torch.as_tensor(vrows, device=cuda_device)].double().cpu().numpy()
+    print(f"{name}: dW on {len(vrows)} vocabulary rows, max err / max|ref| {grad_err(got_dW, ref_dW):.3e}")
+    assert grad_err(got_dW, ref_dW) <= GRAD_FRAC
