@@ -17,8 +17,10 @@ the backward recompute).
    and dW on 256 sampled vocabulary rows, computed from the oracle's own lse
    of all 32768 rows.
 5. The large-vocabulary head at 131072 tokens and the sweep's 262144-token
-   point, too large for the oracle's full forward here: lse, per-row loss and
-   dH on 256 sampled rows with every chunk's first and last row.
+   point, whose oracle forward over every row takes 5-8 minutes: lse, per-row
+   loss and dH on 256 sampled rows with every chunk's first and last row.  An
+   opt-in test (KD_FULL_ORACLE=1) runs that full forward too: total loss, every
+   lse and per-row loss, and dW on 256 sampled vocabulary rows.
 Cases 3-5 also hold dW to dH through eight seeded projection identities
 <W u v^T, dW> = <dH, H v u^T>, which change when any group of dW rows is lost,
 scaled, offset or transposed.
