@@ -119,8 +119,13 @@ struct GemmParams {
   int reduce_add;
   float scale;
   // EPI_GF: row tiles m >= m_split are the forward of the next chunk, whose
-  // H rows start at a_mn0_2, with rows_valid2 rows and sorted cache sidx2/sp2
+  // H rows start at a_mn0_2, with rows_valid2 rows and sorted cache sidx2/sp2.
+  // EPI_FWD_E with m_split > 0: the forward of two chunks in one launch; the
+  // second chunk's kept exponentials go to rows out_row0_2 + ... of the
+  // operand buffer and its softmax partials to rows part_row2 + ... of the
+  // partial arrays.
   int m_split, a_mn0_2, rows_valid2;
+  int out_row0_2, part_row2;
   const int32_t* sidx2;
   const float* sp2;
   // MN-major operands whose tensor map is the 3-D view {64, K rows, MN / 64}:
@@ -266,7 +271,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         decode_tile(P, tile, m, n, s);
         const int kb0 = s * P.kb_per_split;
         const int kb1 = min(P.kb_total, kb0 + P.kb_per_split);
-        const bool next_part = EPI == EPI_GF && m >= P.m_split;  // the next chunk's forward rows
+        // the next chunk's rows (a merged launch)
+        const bool next_part = (EPI == EPI_GF || EPI == EPI_FWD_E) && P.m_split > 0 && m >= P.m_split;
         const int a_row = (next_part ? P.a_mn0_2 + (m - P.m_split) * Cfg::TILE_M : P.a_mn0 + m * Cfg::TILE_M) +
                           static_cast<int>(rank) * BM;
         const int b_row = P.b_mn0 + n * BN + static_cast<int>(rank) * Cfg::B_ROWS;
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t acc_par = (local >> 1) & 1;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       // which epilogue this tile runs: the forward statistics or G (runtime only for EPI_GF)
-      const bool next_part = EPI == EPI_GF && m >= P.m_split;
+      const bool next_part = (EPI == EPI_GF || EPI == EPI_FWD_E) && P.m_split > 0 && m >= P.m_split;
       const bool is_fwd = EPI == EPI_FWD || next_part;
       const int mm = next_part ? m - P.m_split : m;                         // tile row within its chunk
       const int row0 = mm * Cfg::TILE_M + static_cast<int>(rank) * BM;  // first row of D this CTA holds
@@ -552,7 +558,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             fence_proxy_async_smem();
             named_bar_sync(EPI_BAR_ID, EPI_WARPS * 32);
             if (out_leader) {
-              tma_store_2d(&tmD, n * BN + (c >> 1) * G_SLICE_COLS, P.out_row0 + row0, buf);
+              tma_store_2d(&tmD, n * BN + (c >> 1) * G_SLICE_COLS, (next_part ? P.out_row0_2 : P.out_row0) + row0, buf);
               bulk_commit();
             }
             ++slice;
@@ -586,7 +592,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
       if constexpr (EPI == EPI_FWD || EPI == EPI_FWD_E || EPI == EPI_GF) {
         if (rv && (EPI != EPI_GF || is_fwd)) {
-          const size_t o = static_cast<size_t>(n) * P.ld_part + r;
+          const size_t o = static_cast<size_t>(n) * P.ld_part + r + (EPI == EPI_FWD_E && next_part ? P.part_row2 : 0);
           P.part_m[o] = run_m;
           P.part_s[o] = run_s;
           P.part_pz[o] = pz;

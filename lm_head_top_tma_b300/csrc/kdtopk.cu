@@ -219,6 +219,9 @@ struct Plan {
   int tile_m;    // rows per GEMM tile: 256 for pairs, 128 otherwise
   int dw_group;  // chunks whose G rows one dW GEMM consumes (K = dw_group * C)
   int64_t ldg;
+  // leading dimension of the softmax partials: two chunks' rows when the
+  // no-recompute step can run two chunks' forward GEMMs as one launch
+  int part_ld;
   size_t off_status, off_sidx, off_sp, off_M, off_E, off_pm, off_ps, off_pz, off_Lrow, off_G, off_dhp, total;
 };
 
@@ -285,10 +288,11 @@ kd_status make_plan(int64_t T, int d, int V, int K, int chunk, int what, Plan* p
   if (p.prep_bufs == 2) o += p.prep_stride;
   p.off_pm = p.off_ps = p.off_pz = p.off_Lrow = 0;
   p.off_G = p.off_dhp = 0;
+  p.part_ld = ((what & KD_WS_FUSED) == KD_WS_FUSED && p.dw_group % 2 == 0) ? 2 * p.Cpad : p.Cpad;
   if (what & KD_WS_FORWARD) {
-    p.off_pm = take(size_t(p.nt) * p.Cpad * 4);
-    p.off_ps = take(size_t(p.nt) * p.Cpad * 4);
-    p.off_pz = take(size_t(p.nt) * p.Cpad * 4);
+    p.off_pm = take(size_t(p.nt) * p.part_ld * 4);
+    p.off_ps = take(size_t(p.nt) * p.part_ld * 4);
+    p.off_pz = take(size_t(p.nt) * p.part_ld * 4);
     p.off_Lrow = take(size_t(p.Cpad) * 8);
   }
   if (what & KD_WS_BACKWARD) {
@@ -427,6 +431,13 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   auto t0_of = [&](int c) { return int64_t(c) * pl.C; };
   auto rows_of = [&](int c) { return static_cast<int>(std::min<int64_t>(pl.C, T - t0_of(c))); };
   auto gslot_of = [&](int c) { return c % pl.dw_group; };  // chunk c's G rows: [gslot * Cpad, +Cpad)
+  // the no-recompute step runs chunk pairs (c even, c + 1) through one forward
+  // launch when the G slots of a pair are adjacent (an even dW group) and the
+  // partials hold two chunks; the pair's second chunk keeps its partials in the
+  // second half
+  const bool kmerge = keep && (mode & MODE_FWD) && (mode & MODE_BWD) && pl.part_ld == 2 * pl.Cpad &&
+                      pl.prep_bufs == 2 && pl.nchunks > 1 && merge_enabled();
+  auto part_off = [&](int c) { return (kmerge && (c & 1)) ? size_t(pl.Cpad) : size_t(0); };
   // the sorted cache of chunk c lives in prep buffer c % prep_bufs
   auto pbuf = [&](int c, size_t off) { return w8 + off + size_t(c % pl.prep_bufs) * pl.prep_stride; };
   auto sidx_of = [&](int c) { return reinterpret_cast<int32_t*>(pbuf(c, pl.off_sidx)); };
@@ -447,7 +458,7 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
     L.part_m = pm;
     L.part_s = ps;
     L.part_pz = ppz;
-    L.ld_part = pl.Cpad;
+    L.ld_part = pl.part_ld;
     L.out_row0 = gslot_of(c) * pl.Cpad;
     L.rowM = rowM_of(c);
     L.lse = ((mode & MODE_FWD) ? lse : lse_in) + t0_of(c);
@@ -484,9 +495,10 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   };
   auto combine = [&](int c) {
     const int rows = rows_of(c);
+    const size_t po = part_off(c);
     const int slot = prof_begin(KD_K_COMBINE, st);
     kd_combine_kernel<<<static_cast<unsigned>(ceil_div(rows, 32)), COMBINE_WARPS * 32, 0, st>>>(
-        pm, ps, ppz, pl.nt, pl.Cpad, rows, rowM_of(c), rowE_of(c), lse + t0_of(c),
+        pm + po, ps + po, ppz + po, pl.nt, pl.part_ld, rows, rowM_of(c), rowE_of(c), lse + t0_of(c),
         loss_rows ? loss_rows + t0_of(c) : nullptr, Lrow);
     kd_loss_reduce_kernel<<<1, 1024, 0, st>>>(Lrow, rows, loss_acc, c == 0 ? 1 : 0,
                                               c == pl.nchunks - 1 ? loss : nullptr);
@@ -496,11 +508,26 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
       const int gs = prof_begin(KD_K_G_FROM_E, st);
       kd_g_from_e_kernel<<<static_cast<unsigned>(rows), GPASS_THREADS, 0, st>>>(
           G + size_t(gslot_of(c)) * pl.Cpad * pl.ldg, pl.ldg, rows, V, K, sidx_of(c), sp_of(c), rowM_of(c),
-          lse + t0_of(c), pm, pl.Cpad);
+          lse + t0_of(c), pm + po, pl.part_ld);
       e = cudaGetLastError();
       prof_end(gs, st);
     }
     return check(e);
+  };
+  // the no-recompute step: chunks c and c+1's forward GEMMs (kept exponentials)
+  // in one launch, sharing every W tile through L2
+  auto forward_pair = [&](int c) {
+    GemmParams P = logits_params(c);
+    const GemmParams F = logits_params(c + 1);
+    P.m_split = P.num_m;
+    P.num_m = 2 * P.num_m;
+    P.a_mn0_2 = F.a_mn0;
+    P.rows_valid2 = F.rows_valid;
+    P.sidx2 = F.sidx;
+    P.sp2 = F.sp;
+    P.out_row0_2 = F.out_row0;
+    P.part_row2 = pl.Cpad;
+    return check(launch_gemm_any<EPI_FWD_E, false, false>(pr, KD_K_LOGITS_FWD, tmH_k, tmW_k, tmG_k, P, sms, st));
   };
   auto g_gemm = [&](int c) {
     const GemmParams P = logits_params(c);
@@ -561,6 +588,22 @@ kd_status run(int mode, const void* H, const void* W, const int32_t* idx, const 
   };
 
   const bool fused = (mode & MODE_FWD) && (mode & MODE_BWD);
+  if (kmerge) {
+    // no-recompute path: the forward GEMMs of chunks c and c+1 (c even) as one
+    // launch, then each chunk's combine, G pass and backward GEMMs in order
+    for (int c = 0; c < pl.nchunks; c += 2) {
+      const bool pair = c + 1 < pl.nchunks;
+      if (!prep(c)) return KD_ERR_CUDA;
+      if (pair) {
+        if (!prep(c + 1) || !forward_pair(c)) return KD_ERR_CUDA;
+      } else if (!forward_gemm(c)) {
+        return KD_ERR_CUDA;
+      }
+      if (!combine(c) || (pair && !combine(c + 1))) return KD_ERR_CUDA;
+      if (!dh_and_dw(c) || (pair && !dh_and_dw(c + 1))) return KD_ERR_CUDA;
+    }
+    return KD_OK;
+  }
   if (fused && !keep && pl.prep_bufs == 2 && pl.nchunks > 1 && merge_enabled()) {
     // recompute path, software-pipelined by one chunk: after chunk c's forward and
     // combine, chunk c's G GEMM runs together with chunk c+1's forward GEMM
