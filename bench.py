@@ -50,10 +50,10 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 # launch per group of two 2048-row chunks, the first group of a step stores dW
 # ("first"), the others reduce-add into it ("rest").  logits_gf: one chunk's G
 # with the next chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": "3bd9eb916468744c", "kinds": {
-    "gemm_dw": {"first": 1346497792 + 1544325376, "rest": 2748394752 + 1535060480},
-    "logits_gf": {"first": 905059072 + 524794624,
-                  "rest": (924568064 + 523076864 + 920643840 + 522863104) // 2},
+TRAFFIC = {"workload": "longctx", "src_sha": "8d2714378640a39b", "kinds": {
+    "gemm_dw": {"first": 1387356928 + 1544024576, "rest": 2790736128 + 1534004480},
+    "logits_gf": {"first": 884839168 + 525963008,
+                  "rest": (880542976 + 523631872 + 903304448 + 522870528) // 2},
 }}
 # sequence lengths of the peak-bytes-versus-T series (the output-head-only benchmark's range)
 PEAK_T = (4096, 8192, 16384, 32768, 65536, 131072, 262144)
