@@ -164,8 +164,9 @@ bool pair_enabled() {
   return v;
 }
 
-// The recompute fused step runs chunk c's G GEMM and chunk c+1's forward GEMM
-// as one launch; KD_MERGE_LOGITS=0 (read once per process) keeps them apart.
+// The fused steps run two chunks' projections as one launch (chunk c's G GEMM
+// with chunk c+1's forward, or without the recompute the forward GEMMs of
+// chunks c and c+1); KD_MERGE_LOGITS=0 (read once per process) keeps them apart.
 bool merge_enabled() {
   static bool v = [] {
     const char* e = std::getenv("KD_MERGE_LOGITS");
