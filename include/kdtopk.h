@@ -89,7 +89,10 @@ typedef enum kd_status {
  * through ceil(T / chunk) on T: the chunk working set (a [chunk,V] bf16
  * gradient operand and [chunk, V/256] softmax partials) is reused chunk after
  * chunk, so memory grows linearly in T only through the caller's own inputs
- * and outputs.  Returns 0 for invalid sizes.
+ * and outputs.  With KD_WS_FUSED and an even number of chunks per dW group
+ * (below) the partials hold two chunks' rows, so that the step without the
+ * recompute can run two chunks' forward GEMMs as one launch.  Returns 0 for
+ * invalid sizes.
  * When chunk is a multiple of 128 the backward keeps G for a group of
  * consecutive chunks (up to 4096 rows, at most 4 chunks; environment variable
  * KD_DW_GROUP_ROWS, read once per process, changes the row target, 0 turns it
@@ -173,10 +176,12 @@ KD_API kd_status kd_topk_kl_fused_step_norecompute(const void* H, const void* W,
  *     KD_ERR_WORKSPACE before anything is launched (for example chunk 2048
  *     fits both a 128,256- and a 201,088-word vocabulary; chunk 4096 with a
  *     201,088-word vocabulary does not).
+ *   - The call waits for `stream` (below), so it cannot be captured into a
+ *     CUDA graph: kd_topk_kl_forward with a caller workspace is the form to
+ *     capture.
  *   - The first call on a device looks up the scratch array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.  The address is kept for the
- *     life of the process: cudaDeviceReset unloads the array with the
+ *     (cudaGetSymbolAddress) with that device current.  The address is kept
+ *     for the life of the process: cudaDeviceReset unloads the array with the
  *     library's device code, so do not use this entry point across a reset.
  *   - Every call on a device shares the one array and finds the previous
  *     call's contents in it; each call re-initialises what it needs.  Calls
