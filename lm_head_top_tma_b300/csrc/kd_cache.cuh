@@ -6,15 +6,15 @@
 // aimodeling.com "First cut": top-100 probabilities cached for every token),
 // here over logits that are already on the device.
 //
-// One block of 512 threads per row (grid-stride over rows, two blocks per
-// SM); each row is read from HBM once, with 16-byte loads, several in flight
-// per thread, after an L2 prefetch of the row.  A row of up to 256 KB is
-// requested whole when its pass 1 starts; a longer row through a window that
-// keeps the next 128 KB ahead of pass 1 requested, so that the rows two
-// blocks per SM hold in L2 stay well inside it.  Either way the first 64 KB
-// of the block's next row is requested while the block selects this one, so
-// that HBM keeps streaming through the selection (more than that crowds L2):
-//   pass 1  per-slot maximum (1024 slots: two per thread, every element in
+// One block per row (grid-stride over rows): 256-thread blocks, four per SM,
+// for rows of up to 256 KB, 512-thread blocks, two per SM, for longer rows
+// (the block shapes below).  Each row is read from HBM once, with 16-byte
+// loads, several in flight per thread, behind L2 prefetches that keep a
+// window of the row requested ahead of pass 1 (64 KB for the narrow shape,
+// 128 KB for the wide one; the wide shape requests a row of up to 256 KB
+// whole).  The head of the block's next row is requested while the block
+// selects this one, so that HBM keeps streaming through the selection:
+//   pass 1  per-slot maximum (two slots per thread, every element in
 //           exactly one), an online (max, sum of 2^x) for lse, and the maximum
 //           of every 16-byte group, kept in shared memory (as bf16, rounded up
 //           for fp32 logits);
@@ -23,14 +23,15 @@
 //           reduced alongside): at least K distinct elements reach theta, so
 //           every top-K element has key >= theta;
 //   pass 2  only the groups whose maximum reaches theta (typically about K of
-//           them) are listed and read again, from L2, all in flight together,
+//           them) are listed and read again (from L2, unless the narrow
+//           shape's window has moved on), all in flight together,
 //           and their elements >= theta are collected in shared memory (list
 //           and candidates appended with one atomic per warp); they are
 //           ranked by (key descending, id ascending) by counting (bitonic
-//           sort above 1024 candidates);
+//           sort above two candidates per thread);
 //   fallback  rows whose group maxima do not fit in shared memory, or that
 //           cannot be read 16 bytes at a time, are scanned whole in pass 2;
-//           when more than CACHE_CAP elements reach theta (heavily tied or
+//           when more candidates reach theta than the list holds (heavily tied or
 //           adversarial rows) the exact K-th key is found by a binary search
 //           over the key space, and the tied elements at it are taken in
 //           ascending id order by an ordered block scan.
@@ -52,19 +53,33 @@
 
 namespace kd {
 
-constexpr int CACHE_THREADS = 512;
-constexpr int CACHE_SLOTS = 2 * CACHE_THREADS;  // per-row maxima used to bound the K-th key
-constexpr int CACHE_CAP = 4096;                 // candidates kept in shared memory
-constexpr int CACHE_UNROLL = 4;                 // 16-byte loads in flight per thread
-constexpr int CACHE_GMAX = 32768;               // 16-byte group maxima kept in shared memory
-constexpr int CACHE_GLIST = 1024;               // groups listed for the re-read of pass 2
-constexpr int64_t CACHE_WHOLE_ROW = 262144;     // rows up to this many bytes are prefetched whole
-constexpr int64_t CACHE_PF_WINDOW = 131072;     // bytes kept requested ahead of pass 1 in longer rows
-constexpr int64_t CACHE_PF_HEAD = 65536;        // bytes of the next row requested during selection
+constexpr int CACHE_UNROLL = 4;              // 16-byte loads in flight per thread
+constexpr int CACHE_GLIST = 1024;            // groups listed for the re-read of pass 2
+constexpr int64_t CACHE_WHOLE_ROW = 262144;  // the wide shape prefetches rows up to this many bytes whole
 
-// dynamic shared memory of kd_topk_cache_kernel: the candidate list, and the
-// group maxima when rows are read 16 bytes at a time
-constexpr int cache_smem_bytes(bool vec) { return CACHE_CAP * 8 + (vec ? CACHE_GMAX * 2 : 0); }
+// Block shapes.  Rows of at most 256 KB read 16 bytes at a time, with K at
+// most the narrow shape's slot count, run the narrow shape: 256-thread blocks, four per SM, each row requested into L2
+// through a 64 KB window (four resident rows per SM requested whole would not
+// fit in L2).  Other rows run the wide shape: 512-thread blocks, two per SM,
+// a row of up to 256 KB requested whole, a longer one through a 128 KB window.
+// CAP candidates and GMAX 16-byte group maxima are kept in shared memory;
+// HEAD bytes of the block's next row are requested while it selects a row.
+template <int NT_, int MINB_, int CAP_, int GMAX_, bool ALL_WINDOWED_, int64_t WINDOW_, int64_t HEAD_>
+struct CacheShape {
+  static constexpr int NT = NT_;
+  static constexpr int MINB = MINB_;
+  static constexpr int CAP = CAP_;
+  static constexpr int GMAX = GMAX_;
+  static constexpr bool ALL_WINDOWED = ALL_WINDOWED_;
+  static constexpr int64_t WINDOW = WINDOW_;
+  static constexpr int64_t HEAD = HEAD_;
+  static constexpr int SLOTS = 2 * NT_;  // slot maxima per row: theta needs K <= SLOTS
+  // dynamic shared memory: the candidate list, and the group maxima when rows
+  // are read 16 bytes at a time
+  static constexpr int smem_bytes(bool vec) { return CAP * 8 + (vec ? GMAX * 2 : 0); }
+};
+using CacheNarrow = CacheShape<256, 4, 2048, 16384, true, 65536, 32768>;
+using CacheWide = CacheShape<512, 2, 4096, 32768, false, 131072, 65536>;
 
 template <typename T>
 struct LogitTraits;
@@ -199,11 +214,12 @@ struct RowView {
   }
 };
 
-// Appends the candidate (key, id) to the block's list; entries past
-// CACHE_CAP are counted but not stored.
+// Appends the candidate (key, id) to the block's list; entries past CAP are
+// counted but not stored.
+template <int CAP>
 __device__ __forceinline__ void push_cand(uint64_t* cand, int* count, uint32_t key, int id) {
   const int at = atomicAdd(count, 1);
-  if (at < CACHE_CAP) cand[at] = (static_cast<uint64_t>(~key) << 32) | static_cast<uint32_t>(id);
+  if (at < CAP) cand[at] = (static_cast<uint64_t>(~key) << 32) | static_cast<uint32_t>(id);
 }
 
 // Reserves n >= 0 consecutive slots of a shared counter for each lane of the
@@ -224,7 +240,7 @@ __device__ __forceinline__ int warp_reserve(int* counter, int n) {
 }
 
 // One byte-level step of a most-significant-byte-first radix select of the
-// K-th largest of the block's 2 * CACHE_THREADS keys (two per thread), after
+// K-th largest of the block's keys (two per thread), after
 // every thread has counted its keys that share `prefix` into hist[256] by the
 // byte at `shift` and the block has synchronised.  Warp 0 picks the byte b of
 // the K-th largest, stores (b, keys above b's bin) in sel[0..1] and clears
@@ -321,17 +337,17 @@ __device__ __forceinline__ void groups_stats(const typename RV::Raw (&x)[U], flo
   }
 }
 
-template <typename TL, bool VEC>
-__global__ void __launch_bounds__(CACHE_THREADS, 2)
+template <typename TL, bool VEC, typename S>
+__global__ void __launch_bounds__(S::NT, S::MINB)
     kd_topk_cache_kernel(const TL* __restrict__ Z, int64_t T, int V, int K, int32_t* __restrict__ idx_out,
                          float* __restrict__ p_out, float* __restrict__ lse_out) {
   using Tr = LogitTraits<TL>;
   using RV = RowView<TL, VEC>;
   constexpr int PV = RV::PV;
-  constexpr int NW = CACHE_THREADS / 32;
+  constexpr int NW = S::NT / 32;
   extern __shared__ __align__(16) unsigned char cache_smem[];
   uint64_t* cand = reinterpret_cast<uint64_t*>(cache_smem);  // (~key << 32) | id
-  uint16_t* gmax = reinterpret_cast<uint16_t*>(cache_smem + CACHE_CAP * 8);  // used when VEC
+  uint16_t* gmax = reinterpret_cast<uint16_t*>(cache_smem + S::CAP * 8);  // used when VEC
   __shared__ float red_m[32], red_s[32];
   __shared__ int red_i[32];
   __shared__ int hist[256];  // radix-select counts, zero between uses
@@ -341,10 +357,10 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
   __shared__ float s_lse;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < 256; i += CACHE_THREADS) hist[i] = 0;
+  for (int i = tid; i < 256; i += S::NT) hist[i] = 0;
 
   const int64_t row_bytes = static_cast<int64_t>(V) * sizeof(TL);
-  const bool windowed = VEC && row_bytes > CACHE_WHOLE_ROW;
+  const bool windowed = VEC && (S::ALL_WINDOWED || row_bytes > CACHE_WHOLE_ROW);
   // thread 0: bytes of the current row already requested into L2, and of the
   // block's next row (its head, requested during this row's selection)
   int64_t req = 0, req_next = 0;
@@ -358,39 +374,39 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
   for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
     const RV rv{Z + row * static_cast<int64_t>(V), V};
     const int ng = rv.groups();
-    const bool screen = VEC && ng <= CACHE_GMAX;  // group maxima fit in shared memory
+    const bool screen = VEC && ng <= S::GMAX;  // group maxima fit in shared memory
     if constexpr (VEC) {
       if (tid == 0) {
         req = req_next;
         req_next = 0;
-        request_upto(rv.z, windowed ? CACHE_PF_WINDOW : row_bytes);
+        request_upto(rv.z, windowed ? S::WINDOW : row_bytes);
       }
     }
     // ---------------- pass 1: slot maxima, online softmax normaliser, group maxima
     float fslot0 = -INFINITY, fslot1 = -INFINITY;  // two disjoint element sets per thread
     float m = -INFINITY, s = 0.f;
     int it = 0;  // the slot of an iteration alternates
-    for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL, ++it) {
+    for (int g0 = tid; g0 < ng; g0 += S::NT * CACHE_UNROLL, ++it) {
       float& slot = (it & 1) ? fslot1 : fslot0;
       // keep the window ahead of what this iteration reads (16 bytes per group)
       if (windowed && tid == 0)
-        request_upto(rv.z, static_cast<int64_t>(it + 1) * CACHE_THREADS * CACHE_UNROLL * 16 + CACHE_PF_WINDOW);
-      if (g0 + (CACHE_UNROLL - 1) * CACHE_THREADS < ng) {
+        request_upto(rv.z, static_cast<int64_t>(it + 1) * S::NT * CACHE_UNROLL * 16 + S::WINDOW);
+      if (g0 + (CACHE_UNROLL - 1) * S::NT < ng) {
         typename RV::Raw x[CACHE_UNROLL];
         float gm[CACHE_UNROLL];
 #pragma unroll
-        for (int u = 0; u < CACHE_UNROLL; ++u) x[u] = rv.load(g0 + u * CACHE_THREADS);
+        for (int u = 0; u < CACHE_UNROLL; ++u) x[u] = rv.load(g0 + u * S::NT);
         groups_stats<CACHE_UNROLL, RV>(x, gm, m, s, slot);
         if (screen) {
 #pragma unroll
-          for (int u = 0; u < CACHE_UNROLL; ++u) gmax[g0 + u * CACHE_THREADS] = gmax_bits<TL>(gm[u]);
+          for (int u = 0; u < CACHE_UNROLL; ++u) gmax[g0 + u * S::NT] = gmax_bits<TL>(gm[u]);
         }
       } else {
-        for (int u = 0; u < CACHE_UNROLL && g0 + u * CACHE_THREADS < ng; ++u) {
-          const typename RV::Raw x[1] = {rv.load(g0 + u * CACHE_THREADS)};
+        for (int u = 0; u < CACHE_UNROLL && g0 + u * S::NT < ng; ++u) {
+          const typename RV::Raw x[1] = {rv.load(g0 + u * S::NT)};
           float gm[1];
           groups_stats<1, RV>(x, gm, m, s, slot);
-          if (screen) gmax[g0 + u * CACHE_THREADS] = gmax_bits<TL>(gm[0]);
+          if (screen) gmax[g0 + u * S::NT] = gmax_bits<TL>(gm[0]);
         }
       }
     }
@@ -400,7 +416,7 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lse_merge(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
     __syncthreads();  // the previous row's shared state is no longer read (and hist is clear)
-    // ---------------- theta: the K-th largest of the 1024 slot maxima, by radix
+    // ---------------- theta: the K-th largest of the slot maxima, by radix
     // select one byte at a time; the block's lse is reduced alongside
     if (lane == 0) {
       red_m[warp] = m;
@@ -436,7 +452,7 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
     if constexpr (VEC) {
       // the head of the block's next row into L2 while this row's selection runs
       if (tid == 0 && row + gridDim.x < T) {
-        req_next = min(row_bytes, CACHE_PF_HEAD);
+        req_next = min(row_bytes, S::HEAD);
         prefetch_l2_bulk(rv.z + static_cast<int64_t>(gridDim.x) * V, req_next);
       }
     }
@@ -450,7 +466,7 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       // smallest bf16 >= theta's value
       const __nv_bfloat162 th2 = __bfloat162bfloat162(__float2bfloat16_ru(tv));
       const int nv = (ng + 7) / 8;
-      for (int v0 = warp * 32; v0 < nv; v0 += CACHE_THREADS) {  // v = tid + k CACHE_THREADS
+      for (int v0 = warp * 32; v0 < nv; v0 += S::NT) {  // v = tid + k S::NT
         const int v = v0 + lane;
         uint32_t m8 = 0;  // bit e: group v * 8 + e reaches theta
         if (v < nv) {
@@ -474,13 +490,13 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
             RV::floats(rv.load(g), f);
 #pragma unroll
             for (int i = 0; i < PV; ++i)
-              if (f[i] >= tv) push_cand(cand, &s_count, Tr::fkey(f[i]), g * PV + i);
+              if (f[i] >= tv) push_cand<S::CAP>(cand, &s_count, Tr::fkey(f[i]), g * PV + i);
           }
         }
       }
       __syncthreads();
       const int nl = min(s_groups, CACHE_GLIST);
-      for (int i0 = warp * 32; i0 < nl; i0 += CACHE_THREADS) {  // i = tid + k CACHE_THREADS
+      for (int i0 = warp * 32; i0 < nl; i0 += S::NT) {  // i = tid + k S::NT
         const int i = i0 + lane;
         const int g = i < nl ? glist[i] : 0;
         float f[PV];
@@ -494,19 +510,19 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
 #pragma unroll
         for (int e = 0; e < PV; ++e)
           if ((mk >> e) & 1u) {
-            if (at < CACHE_CAP) cand[at] = (static_cast<uint64_t>(~Tr::fkey(f[e])) << 32) | static_cast<uint32_t>(g * PV + e);
+            if (at < S::CAP) cand[at] = (static_cast<uint64_t>(~Tr::fkey(f[e])) << 32) | static_cast<uint32_t>(g * PV + e);
             ++at;
           }
       }
     } else {
-      for (int g0 = tid; g0 < ng; g0 += CACHE_THREADS * CACHE_UNROLL) {
+      for (int g0 = tid; g0 < ng; g0 += S::NT * CACHE_UNROLL) {
         typename RV::Raw x[CACHE_UNROLL];
 #pragma unroll
         for (int u = 0; u < CACHE_UNROLL; ++u)
-          if (g0 + u * CACHE_THREADS < ng) x[u] = rv.load(g0 + u * CACHE_THREADS);
+          if (g0 + u * S::NT < ng) x[u] = rv.load(g0 + u * S::NT);
 #pragma unroll
         for (int u = 0; u < CACHE_UNROLL; ++u) {
-          const int g = g0 + u * CACHE_THREADS;
+          const int g = g0 + u * S::NT;
           if (g >= ng) break;
           if constexpr (VEC) {
             if (!(Tr::group_max(x[u]) >= tv)) continue;  // the common case: no candidate in the group
@@ -515,20 +531,20 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
           RV::floats(x[u], f);
 #pragma unroll
           for (int i = 0; i < PV; ++i)
-            if (f[i] >= tv) push_cand(cand, &s_count, Tr::fkey(f[i]), g * PV + i);
+            if (f[i] >= tv) push_cand<S::CAP>(cand, &s_count, Tr::fkey(f[i]), g * PV + i);
         }
       }
     }
     __syncthreads();
     int n = s_count;
-    if (n > CACHE_CAP) {
+    if (n > S::CAP) {
       // ---------------- fallback: exact K-th key by binary search, then ordered ties
       // largest kappa with count(key >= kappa) >= K, searched in [theta, 2^bits - 1]
       uint64_t lo2 = theta, hi2 = (Tr::KEY_BITS == 32) ? 0xFFFFFFFFull : 0xFFFFull;
       while (lo2 < hi2) {
         const uint64_t mid = lo2 + (hi2 - lo2 + 1) / 2;
         int cnt = 0;
-        for (int j = tid; j < V; j += CACHE_THREADS) cnt += static_cast<uint64_t>(Tr::key(rv.z[j])) >= mid;
+        for (int j = tid; j < V; j += S::NT) cnt += static_cast<uint64_t>(Tr::key(rv.z[j])) >= mid;
         if (block_sum_int(cnt, red_i) >= K) lo2 = mid;
         else hi2 = mid - 1;
       }
@@ -536,14 +552,14 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       __syncthreads();
       if (tid == 0) s_count = 0;
       __syncthreads();
-      for (int j = tid; j < V; j += CACHE_THREADS) {  // fewer than K are strictly above kappa
+      for (int j = tid; j < V; j += S::NT) {  // fewer than K are strictly above kappa
         const uint32_t k = Tr::key(rv.z[j]);
         if (k > kappa) cand[atomicAdd(&s_count, 1)] = (static_cast<uint64_t>(~k) << 32) | static_cast<uint32_t>(j);
       }
       __syncthreads();
       int taken = s_count;
       // ties at kappa in ascending id order, one block-wide segment at a time
-      for (int base = 0; base < V && taken < K; base += CACHE_THREADS) {
+      for (int base = 0; base < V && taken < K; base += S::NT) {
         const int j = base + tid;
         const bool tie = j < V && Tr::key(rv.z[j]) == kappa;
         const unsigned bal = __ballot_sync(0xffffffffu, tie);
@@ -569,11 +585,11 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       idx_out[row * K + k] = static_cast<int>(c & 0xFFFFFFFFu);
       p_out[row * K + k] = ex2((z - lse) * kLog2e);
     };
-    if (n <= CACHE_THREADS / 2) {
+    if (n <= S::NT / 2) {
       // rank of each candidate = number of smaller composite keys (all distinct),
       // counted by P lanes of one warp
       int P = 1;
-      while (P < 32 && 2 * P * n <= CACHE_THREADS) P *= 2;
+      while (P < 32 && 2 * P * n <= S::NT) P *= 2;
       const int c = tid / P, part = tid % P;
       const uint64_t mine = c < n ? cand[c] : ~0ull;
       int rank = 0;
@@ -583,14 +599,14 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       }
       for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
       if (c < n && part == 0 && rank < K) emit(mine, rank);
-    } else if (n <= 2 * CACHE_THREADS) {
+    } else if (n <= 2 * S::NT) {
       // rank of each candidate = number of smaller composite keys (all distinct)
       uint64_t mine[2];
       int rank[2] = {0, 0};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) mine[h] = (tid + h * CACHE_THREADS < n) ? cand[tid + h * CACHE_THREADS] : ~0ull;
+      for (int h = 0; h < 2; ++h) mine[h] = (tid + h * S::NT < n) ? cand[tid + h * S::NT] : ~0ull;
       if (tid < n) {  // only candidate owners count
-        if (tid + CACHE_THREADS < n) {
+        if (tid + S::NT < n) {
           for (int j = 0; j < n; ++j) {
             const uint64_t cj = cand[j];
             rank[0] += cj < mine[0];
@@ -602,14 +618,14 @@ __global__ void __launch_bounds__(CACHE_THREADS, 2)
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        if (tid + h * CACHE_THREADS < n && rank[h] < K) emit(mine[h], rank[h]);
+        if (tid + h * S::NT < n && rank[h] < K) emit(mine[h], rank[h]);
     } else {
       int n_pad = 1;
       while (n_pad < n) n_pad <<= 1;
-      for (int i = n + tid; i < n_pad; i += CACHE_THREADS) cand[i] = ~0ull;
+      for (int i = n + tid; i < n_pad; i += S::NT) cand[i] = ~0ull;
       __syncthreads();
       block_bitonic_sort_u64(cand, n_pad);
-      for (int k = tid; k < K; k += CACHE_THREADS) emit(cand[k], k);
+      for (int k = tid; k < K; k += S::NT) emit(cand[k], k);
     }
     if (tid == 0 && lse_out) lse_out[row] = lse;
   }

@@ -28,6 +28,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include "kd_aux.cuh"
@@ -690,28 +691,32 @@ kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, in
   const int sms = current_sm_count();
   const int slot = prof_begin(KD_K_OTHER, st);
   cudaError_t e = cudaSuccess;
-  const int smem = cache_smem_bytes(vec);
-  auto run_kernel = [&](auto kern, const auto* z) {
+  // the narrow block shape for rows of at most 256 KB read 16 bytes at a time,
+  // when its slot maxima can bound the K-th key (K <= its slot count)
+  const bool narrow = vec && int64_t(V) * (logits_bf16 ? 2 : 4) <= CACHE_WHOLE_ROW && K <= CacheNarrow::SLOTS;
+  auto run_kernel = [&](auto kern, const auto* z, int threads, int smem) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CACHE_THREADS, smem) != cudaSuccess || per_sm < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1) {
       cudaGetLastError();
       per_sm = 1;
     }
     const int blocks = static_cast<int>(std::min<int64_t>(T, int64_t(per_sm) * sms));
-    kern<<<blocks, CACHE_THREADS, smem, st>>>(z, T, V, K, idx, p, lse);
+    kern<<<blocks, threads, smem, st>>>(z, T, V, K, idx, p, lse);
     e = cudaGetLastError();
   };
-  if (logits_bf16) {
-    const auto* z = static_cast<const __nv_bfloat16*>(logits);
-    if (vec) run_kernel(kd_topk_cache_kernel<__nv_bfloat16, true>, z);
-    else run_kernel(kd_topk_cache_kernel<__nv_bfloat16, false>, z);
-  } else {
-    const auto* z = static_cast<const float*>(logits);
-    if (vec) run_kernel(kd_topk_cache_kernel<float, true>, z);
-    else run_kernel(kd_topk_cache_kernel<float, false>, z);
-  }
+  auto run_typed = [&](const auto* z) {
+    using TL = std::remove_const_t<std::remove_pointer_t<decltype(z)>>;
+    if (narrow)
+      run_kernel(kd_topk_cache_kernel<TL, true, CacheNarrow>, z, CacheNarrow::NT, CacheNarrow::smem_bytes(true));
+    else if (vec)
+      run_kernel(kd_topk_cache_kernel<TL, true, CacheWide>, z, CacheWide::NT, CacheWide::smem_bytes(true));
+    else
+      run_kernel(kd_topk_cache_kernel<TL, false, CacheWide>, z, CacheWide::NT, CacheWide::smem_bytes(false));
+  };
+  if (logits_bf16) run_typed(static_cast<const __nv_bfloat16*>(logits));
+  else run_typed(static_cast<const float*>(logits));
   prof_end(slot, st);
   return e == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }

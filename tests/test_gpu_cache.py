@@ -16,7 +16,8 @@ groups: bf16 rows up to V = 262144, fp32 rows up to V = 131072) and re-reads
 only the groups that can hold a top-K element; the placement cases put the
 top K at the row's end, its start, in one run, scattered, and the capacity
 cases take rows at and just past the largest V it covers (longer rows are
-scanned whole)."""
+scanned whole), rows on both sides of the switch between its two block shapes
+(256 KB rows), and candidate lists at and one past each shape's capacity."""
 import numpy as np
 import pytest
 import torch
@@ -55,6 +56,7 @@ def test_teacher_like_rows(cuda_device, dtype, V, K):
 
 
 @pytest.mark.parametrize("T,V,K", [(5, 300, 5), (3, 64, 64), (7, 1000, 1), (4, 5000, 1024), (2, 1024, 1024),
+                                   (4, 5000, 512), (4, 5000, 513),  # the narrow shape's 512 slots bound K <= 512
                                    (1, 1, 1), (9, 2047, 33),
                                    (3000, 520, 7),       # many short rows per block
                                    (700, 16392, 100)])   # rows of two chunks, the second nearly empty
@@ -135,6 +137,32 @@ def test_rows_around_group_maxima_capacity(cuda_device, dtype, V):
     length is not a multiple of 16 bytes (element-wise loads)."""
     Z = make_teacher_logits(6, V, seed=V, device=cuda_device, dtype=dtype)
     check(Z, 100)
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 131072), ("bf16", 131080), ("fp32", 65536), ("fp32", 65540)])
+def test_rows_around_the_block_shape_switch(cuda_device, dtype, V):
+    """Rows of exactly 256 KB (the narrow block shape: 256 threads, four blocks
+    per SM, a 64 KB prefetch window) and one 16-byte group longer (the wide
+    shape: 512 threads, two per SM)."""
+    Z = make_teacher_logits(6, V, seed=V + 1, device=cuda_device, dtype=dtype)
+    check(Z, 100)
+
+
+@pytest.mark.parametrize("V,n_eq", [(20000, 2048), (20000, 2049), (150000, 4096), (150000, 4097)])
+def test_candidate_list_capacity(cuda_device, V, n_eq):
+    """n_eq equal maxima in one run: every one of them reaches theta, so the
+    candidate list holds exactly n_eq entries.  The narrow shape (a 40 KB row)
+    keeps 2048, the wide shape (a 300 KB row) 4096; one more takes the exact
+    fallback."""
+    Z = make_teacher_logits(3, V, seed=n_eq, device=cuda_device, dtype="bf16")
+    top = float(Z.float().max()) + 2.0
+    Z[0, 777:777 + n_eq] = top
+    Z[1, V - n_eq:] = top
+    Z[2, 0:n_eq] = top
+    idx, _ = check(Z, 100)
+    assert idx[0].tolist() == list(range(777, 877))
+    assert idx[1].tolist() == list(range(V - n_eq, V - n_eq + 100))
+    assert idx[2].tolist() == list(range(100))
 
 
 @pytest.mark.parametrize("K", [1, 16, 17, 512, 1024])
