@@ -58,12 +58,13 @@ constexpr int CACHE_GLIST = 1024;            // groups listed for the re-read of
 constexpr int64_t CACHE_WHOLE_ROW = 262144;  // the wide shape prefetches rows up to this many bytes whole
 
 // Block shapes.  Rows of at most 256 KB read 16 bytes at a time, with K at
-// most the narrow shape's slot count, run the narrow shape: 256-thread blocks, four per SM, each row requested into L2
-// through a 64 KB window (four resident rows per SM requested whole would not
-// fit in L2).  Other rows run the wide shape: 512-thread blocks, two per SM,
-// a row of up to 256 KB requested whole, a longer one through a 128 KB window.
-// CAP candidates and GMAX 16-byte group maxima are kept in shared memory;
-// HEAD bytes of the block's next row are requested while it selects a row.
+// most the narrow shape's slot count, run the narrow shape: 256-thread
+// blocks, four per SM, each row requested into L2 through a 64 KB window
+// (four resident rows per SM requested whole would not fit in L2).  Other
+// rows run the wide shape: 512-thread blocks, two per SM, a row of up to
+// 256 KB requested whole, a longer one through a 128 KB window.  CAP
+// candidates and GMAX 16-byte group maxima are kept in shared memory; HEAD
+// bytes of the block's next row are requested while it selects a row.
 template <int NT_, int MINB_, int CAP_, int GMAX_, bool ALL_WINDOWED_, int64_t WINDOW_, int64_t HEAD_>
 struct CacheShape {
   static constexpr int NT = NT_;
