@@ -50,10 +50,10 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 # launch per group of two 2048-row chunks, the first group of a step stores dW
 # ("first"), the others reduce-add into it ("rest").  logits_gf: one chunk's G
 # with the next chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": "8d2714378640a39b", "kinds": {
-    "gemm_dw": {"first": 1387356928 + 1544024576, "rest": 2790736128 + 1534004480},
-    "logits_gf": {"first": 884839168 + 525963008,
-                  "rest": (880542976 + 523631872 + 903304448 + 522870528) // 2},
+TRAFFIC = {"workload": "longctx", "src_sha": "fe2b7aafccd2f51b", "kinds": {
+    "gemm_dw": {"first": 1370842624 + 1545507072, "rest": 2743538432 + 1534056192},
+    "logits_gf": {"first": 858305792 + 525309952,
+                  "rest": (852527360 + 522702080 + 862584576 + 522403072) // 2},
 }}
 # sequence lengths of the peak-bytes-versus-T series (the output-head-only benchmark's range)
 PEAK_T = (4096, 8192, 16384, 32768, 65536, 131072, 262144)
