@@ -65,7 +65,7 @@ constexpr int64_t CACHE_WHOLE_ROW = 262144;  // the wide shape prefetches rows u
 // 256 KB requested whole, a longer one through a 128 KB window.  CAP
 // candidates and GMAX 16-byte group maxima are kept in shared memory; HEAD
 // bytes of the block's next row are requested while it selects a row.
-template <int NT_, int MINB_, int CAP_, int GMAX_, bool ALL_WINDOWED_, int64_t WINDOW_, int64_t HEAD_>
+template <int NT_, int MINB_, int CAP_, int GMAX_, bool ALL_WINDOWED_, int64_t WINDOW_, int64_t HEAD_, int VB_ = 16>
 struct CacheShape {
   static constexpr int NT = NT_;
   static constexpr int MINB = MINB_;
@@ -75,12 +75,18 @@ struct CacheShape {
   static constexpr int64_t WINDOW = WINDOW_;
   static constexpr int64_t HEAD = HEAD_;
   static constexpr int SLOTS = 2 * NT_;  // slot maxima per row: theta needs K <= SLOTS
+  // bytes per vector load of rows read in vectors (16, or 32 with one group
+  // maximum per 32 bytes), and vector loads in flight per thread
+  static constexpr int VB = VB_;
+  static constexpr int UNR = VB_ == 32 ? 2 : 4;
   // dynamic shared memory: the candidate list, and the group maxima when rows
   // are read 16 bytes at a time
   static constexpr int smem_bytes(bool vec) { return CAP * 8 + (vec ? GMAX * 2 : 0); }
 };
 using CacheNarrow = CacheShape<256, 4, 2048, 16384, true, 65536, 32768>;
+using CacheNarrow32 = CacheShape<256, 4, 2048, 16384, true, 65536, 32768, 32>;
 using CacheWide = CacheShape<512, 2, 4096, 32768, false, 131072, 65536>;
+using CacheWide32 = CacheShape<512, 2, 4096, 32768, false, 131072, 65536, 32>;
 
 template <typename T>
 struct LogitTraits;
@@ -110,6 +116,8 @@ struct LogitTraits<float> {
   __device__ static float group_max(const uint4& r) {
     return fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)), fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
   }
+  // maximum of a 32-byte group
+  __device__ static float group_max2(const uint4& a, const uint4& b) { return fmaxf(group_max(a), group_max(b)); }
 };
 
 template <>
@@ -141,6 +149,14 @@ struct LogitTraits<__nv_bfloat16> {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
     const __nv_bfloat162 a = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
     return fmaxf(__low2float(a), __high2float(a));
+  }
+  // maximum of a 32-byte group
+  __device__ static float group_max2(const uint4& a, const uint4& b) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* k = reinterpret_cast<const __nv_bfloat162*>(&b);
+    const __nv_bfloat162 x = __hmax2(__hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])),
+                                     __hmax2(__hmax2(k[0], k[1]), __hmax2(k[2], k[3])));
+    return fmaxf(__low2float(x), __high2float(x));
   }
 };
 
@@ -187,17 +203,32 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = mn;
 }
 
-// Element-wise access to one row, as 16-byte vectors when the row allows it;
-// a loaded group stays packed (Raw) until its elements are used.
-template <typename TL, bool VEC>
+// 32 bytes of a row, loaded by one 256-bit load
+struct Vec32 {
+  uint4 a, b;
+};
+
+__device__ __forceinline__ Vec32 ldg_v32(const void* p) {
+  Vec32 r;
+  asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w), "=r"(r.b.x), "=r"(r.b.y), "=r"(r.b.z), "=r"(r.b.w)
+      : "l"(p));
+  return r;
+}
+
+// Element-wise access to one row, as VB-byte vectors (16 or 32) when the row
+// allows it; a loaded group stays packed (Raw) until its elements are used.
+template <typename TL, bool VEC, int VB = 16>
 struct RowView {
   const TL* z;
   int V;
-  static constexpr int PV = VEC ? LogitTraits<TL>::PER_VEC : 1;
-  using Raw = typename std::conditional<VEC, uint4, TL>::type;
-  __device__ int groups() const { return VEC ? V / PV : V; }  // VEC rows are whole 16-byte groups
+  static constexpr int PV16 = LogitTraits<TL>::PER_VEC;  // elements per 16 bytes
+  static constexpr int PV = VEC ? PV16 * (VB / 16) : 1;
+  using Raw = typename std::conditional<VEC, typename std::conditional<VB == 32, Vec32, uint4>::type, TL>::type;
+  __device__ int groups() const { return VEC ? V / PV : V; }  // VEC rows are whole groups
   __device__ Raw load(int g) const {
-    if constexpr (VEC) return __ldg(reinterpret_cast<const uint4*>(z) + g);
+    if constexpr (VEC && VB == 32) return ldg_v32(reinterpret_cast<const char*>(z) + static_cast<size_t>(g) * 32);
+    else if constexpr (VEC) return __ldg(reinterpret_cast<const uint4*>(z) + g);
     else return z[g];
   }
   __device__ static TL elem(const Raw& r, int i) {
@@ -205,12 +236,19 @@ struct RowView {
     else return r;
   }
   __device__ static void floats(const Raw& r, float (&f)[PV]) {
-    if constexpr (VEC) LogitTraits<TL>::unpack(r, f);
-    else f[0] = LogitTraits<TL>::value(r);
+    if constexpr (VEC && VB == 32) {
+      LogitTraits<TL>::unpack(r.a, *reinterpret_cast<float(*)[PV16]>(&f[0]));
+      LogitTraits<TL>::unpack(r.b, *reinterpret_cast<float(*)[PV16]>(&f[PV16]));
+    } else if constexpr (VEC) {
+      LogitTraits<TL>::unpack(r, f);
+    } else {
+      f[0] = LogitTraits<TL>::value(r);
+    }
   }
   // the largest value of a loaded group
   __device__ static float gmax(const Raw& r) {
-    if constexpr (VEC) return LogitTraits<TL>::group_max(r);
+    if constexpr (VEC && VB == 32) return LogitTraits<TL>::group_max2(r.a, r.b);
+    else if constexpr (VEC) return LogitTraits<TL>::group_max(r);
     else return LogitTraits<TL>::value(r);
   }
 };
@@ -343,7 +381,8 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
     kd_topk_cache_kernel(const TL* __restrict__ Z, int64_t T, int V, int K, int32_t* __restrict__ idx_out,
                          float* __restrict__ p_out, float* __restrict__ lse_out) {
   using Tr = LogitTraits<TL>;
-  using RV = RowView<TL, VEC>;
+  using RV = RowView<TL, VEC, S::VB>;
+  constexpr int UNR = VEC ? S::UNR : CACHE_UNROLL;  // loads in flight per thread
   constexpr int PV = RV::PV;
   constexpr int NW = S::NT / 32;
   extern __shared__ __align__(16) unsigned char cache_smem[];
@@ -387,23 +426,23 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
     float fslot0 = -INFINITY, fslot1 = -INFINITY;  // two disjoint element sets per thread
     float m = -INFINITY, s = 0.f;
     int it = 0;  // the slot of an iteration alternates
-    for (int g0 = tid; g0 < ng; g0 += S::NT * CACHE_UNROLL, ++it) {
+    for (int g0 = tid; g0 < ng; g0 += S::NT * UNR, ++it) {
       float& slot = (it & 1) ? fslot1 : fslot0;
       // keep the window ahead of what this iteration reads (16 bytes per group)
       if (windowed && tid == 0)
-        request_upto(rv.z, static_cast<int64_t>(it + 1) * S::NT * CACHE_UNROLL * 16 + S::WINDOW);
-      if (g0 + (CACHE_UNROLL - 1) * S::NT < ng) {
-        typename RV::Raw x[CACHE_UNROLL];
-        float gm[CACHE_UNROLL];
+        request_upto(rv.z, static_cast<int64_t>(it + 1) * S::NT * UNR * S::VB + S::WINDOW);
+      if (g0 + (UNR - 1) * S::NT < ng) {
+        typename RV::Raw x[UNR];
+        float gm[UNR];
 #pragma unroll
-        for (int u = 0; u < CACHE_UNROLL; ++u) x[u] = rv.load(g0 + u * S::NT);
-        groups_stats<CACHE_UNROLL, RV>(x, gm, m, s, slot);
+        for (int u = 0; u < UNR; ++u) x[u] = rv.load(g0 + u * S::NT);
+        groups_stats<UNR, RV>(x, gm, m, s, slot);
         if (screen) {
 #pragma unroll
-          for (int u = 0; u < CACHE_UNROLL; ++u) gmax[g0 + u * S::NT] = gmax_bits<TL>(gm[u]);
+          for (int u = 0; u < UNR; ++u) gmax[g0 + u * S::NT] = gmax_bits<TL>(gm[u]);
         }
       } else {
-        for (int u = 0; u < CACHE_UNROLL && g0 + u * S::NT < ng; ++u) {
+        for (int u = 0; u < UNR && g0 + u * S::NT < ng; ++u) {
           const typename RV::Raw x[1] = {rv.load(g0 + u * S::NT)};
           float gm[1];
           groups_stats<1, RV>(x, gm, m, s, slot);
@@ -516,17 +555,17 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
           }
       }
     } else {
-      for (int g0 = tid; g0 < ng; g0 += S::NT * CACHE_UNROLL) {
-        typename RV::Raw x[CACHE_UNROLL];
+      for (int g0 = tid; g0 < ng; g0 += S::NT * UNR) {
+        typename RV::Raw x[UNR];
 #pragma unroll
-        for (int u = 0; u < CACHE_UNROLL; ++u)
+        for (int u = 0; u < UNR; ++u)
           if (g0 + u * S::NT < ng) x[u] = rv.load(g0 + u * S::NT);
 #pragma unroll
-        for (int u = 0; u < CACHE_UNROLL; ++u) {
+        for (int u = 0; u < UNR; ++u) {
           const int g = g0 + u * S::NT;
           if (g >= ng) break;
           if constexpr (VEC) {
-            if (!(Tr::group_max(x[u]) >= tv)) continue;  // the common case: no candidate in the group
+            if (!(RV::gmax(x[u]) >= tv)) continue;  // the common case: no candidate in the group
           }
           float f[PV];
           RV::floats(x[u], f);

@@ -692,8 +692,14 @@ kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, in
   const int slot = prof_begin(KD_K_OTHER, st);
   cudaError_t e = cudaSuccess;
   // the narrow block shape for rows of at most 256 KB read 16 bytes at a time,
-  // when its slot maxima can bound the K-th key (K <= its slot count)
-  const bool narrow = vec && int64_t(V) * (logits_bf16 ? 2 : 4) <= CACHE_WHOLE_ROW && K <= CacheNarrow::SLOTS;
+  // when its slot maxima can bound the K-th key (K <= its slot count); with
+  // 32-byte loads when every row starts on a 32-byte boundary
+  const int64_t row_bytes = int64_t(V) * (logits_bf16 ? 2 : 4);
+  const bool v32 = vec && (reinterpret_cast<uintptr_t>(logits) & 31u) == 0 && row_bytes % 32 == 0;
+  const bool narrow32 = v32 && row_bytes <= 2 * CACHE_WHOLE_ROW && K <= CacheNarrow32::SLOTS;
+  const bool narrow = vec && row_bytes <= CACHE_WHOLE_ROW && K <= CacheNarrow::SLOTS;
+  // rows whose 16-byte group maxima would not fit the wide shape's shared memory
+  const bool wide32 = v32 && row_bytes > int64_t(CacheWide::GMAX) * 16;
   auto run_kernel = [&](auto kern, const auto* z, int threads, int smem) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return;
@@ -708,8 +714,12 @@ kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, in
   };
   auto run_typed = [&](const auto* z) {
     using TL = std::remove_const_t<std::remove_pointer_t<decltype(z)>>;
-    if (narrow)
+    if (narrow32)
+      run_kernel(kd_topk_cache_kernel<TL, true, CacheNarrow32>, z, CacheNarrow32::NT, CacheNarrow32::smem_bytes(true));
+    else if (narrow)
       run_kernel(kd_topk_cache_kernel<TL, true, CacheNarrow>, z, CacheNarrow::NT, CacheNarrow::smem_bytes(true));
+    else if (wide32)
+      run_kernel(kd_topk_cache_kernel<TL, true, CacheWide32>, z, CacheWide32::NT, CacheWide32::smem_bytes(true));
     else if (vec)
       run_kernel(kd_topk_cache_kernel<TL, true, CacheWide>, z, CacheWide::NT, CacheWide::smem_bytes(true));
     else

@@ -11,13 +11,13 @@ a wrong base or a wrong id moves it by orders of magnitude).  Cases: teacher-
 like bf16 and fp32 rows at the workloads' vocabulary sizes, V below the block
 size, K = 1, K = V, K = 1024, heavily tied rows, rows that force the exact
 fallback (thousands of equal maxima, all-equal rows), and masked -inf logits.
-The builder keeps every 16-byte group's maximum in shared memory (up to 32768
-groups: bf16 rows up to V = 262144, fp32 rows up to V = 131072) and re-reads
-only the groups that can hold a top-K element; the placement cases put the
-top K at the row's end, its start, in one run, scattered, and the capacity
-cases take rows at and just past the largest V it covers (longer rows are
-scanned whole), rows on both sides of the switch between its two block shapes
-(256 KB rows), and candidate lists at and one past each shape's capacity."""
+The builder keeps the maximum of every 32-byte group (16-byte group when the
+row is not a multiple of 32 bytes) in shared memory and re-reads only the
+groups that can hold a top-K element; the placement cases put the top K at the
+row's end, its start, in one run, scattered, and the capacity cases take rows
+at and just past the largest V each block shape and load width covers (longer
+rows are scanned whole), and candidate lists at and one past each shape's
+capacity."""
 import numpy as np
 import pytest
 import torch
@@ -106,7 +106,7 @@ def test_full_size_sampled_rows(cuda_device):
     check(Z, 100, rows=np.sort(rng.choice(2048, 48, replace=False)))
 
 
-GMAX_GROUPS = 32768  # 16-byte group maxima kept in shared memory
+GMAX_GROUPS = 32768  # the wide shape's 16-byte group maxima (the narrow shape holds 16384 32-byte ones)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
@@ -132,28 +132,59 @@ def test_topk_placement(cuda_device, dtype):
                                      ("bf16", GMAX_GROUPS * 8 - 3), ("fp32", GMAX_GROUPS * 4),
                                      ("fp32", GMAX_GROUPS * 4 + 4)])
 def test_rows_around_group_maxima_capacity(cuda_device, dtype, V):
-    """Rows with exactly as many 16-byte groups as shared memory holds maxima
-    for, one group more (scanned whole), and a bf16 row just short of it whose
+    """512 KB rows (32-byte loads, the narrow shape's group maxima exactly
+    full), rows 16 bytes longer (16-byte loads, one group past the wide shape's
+    32768 maxima: scanned whole), and a bf16 row just short of 512 KB whose
     length is not a multiple of 16 bytes (element-wise loads)."""
     Z = make_teacher_logits(6, V, seed=V, device=cuda_device, dtype=dtype)
     check(Z, 100)
 
 
-@pytest.mark.parametrize("dtype,V", [("bf16", 131072), ("bf16", 131080), ("fp32", 65536), ("fp32", 65540)])
-def test_rows_around_the_block_shape_switch(cuda_device, dtype, V):
-    """Rows of exactly 256 KB (the narrow block shape: 256 threads, four blocks
-    per SM, a 64 KB prefetch window) and one 16-byte group longer (the wide
-    shape: 512 threads, two per SM)."""
-    Z = make_teacher_logits(6, V, seed=V + 1, device=cuda_device, dtype=dtype)
+# (dtype, V): the block shape and row access each row gets
+SHAPE_ROWS = [
+    ("bf16", 131072),   # 256 KB, 32-byte multiple: narrow shape, 32-byte loads
+    ("bf16", 131064),   # a 16-byte but not 32-byte multiple: narrow shape, 16-byte loads, 16383 groups
+    ("bf16", 131080),   # 16 bytes past 256 KB, not a 32-byte multiple: wide shape, 16-byte loads
+    ("bf16", 262144),   # 512 KB: narrow shape, 32-byte loads, exactly its 16384 group maxima
+    ("bf16", 262160),   # 32 bytes more: wide shape, 32-byte loads
+    ("fp32", 131072),   # 512 KB of fp32: narrow shape, 32-byte loads, at capacity
+    ("fp32", 131080),   # wide shape, 32-byte loads
+    ("bf16", 524288),   # 1 MB: wide shape, 32-byte loads, exactly its 32768 group maxima
+    ("bf16", 524304),   # one 32-byte group more: scanned whole
+]
+
+
+@pytest.mark.parametrize("dtype,V", SHAPE_ROWS)
+def test_rows_around_the_block_shape_switches(cuda_device, dtype, V):
+    """Rows on both sides of every switch between the block shapes (256
+    threads, four blocks per SM, for rows of up to 512 KB; 512 threads, two per
+    SM, above) and the load widths (32-byte loads when the row is a multiple of
+    32 bytes, 16-byte loads otherwise), at and one group past each shape's
+    group-maxima capacity."""
+    Z = make_teacher_logits(4, V, seed=V + 1, device=cuda_device, dtype=dtype)
     check(Z, 100)
 
 
-@pytest.mark.parametrize("V,n_eq", [(20000, 2048), (20000, 2049), (150000, 4096), (150000, 4097)])
+def test_rows_on_a_16_byte_boundary_only(cuda_device):
+    """Rows whose start is 16- but not 32-byte aligned take the 16-byte loads:
+    512 KB bf16 rows then fill the wide shape's 32768 group maxima exactly."""
+    T, V = 4, 262144
+    Z0 = make_teacher_logits(T, V, seed=9, device=cuda_device, dtype="bf16")
+    buf = torch.empty(T * V + 8, device=cuda_device, dtype=torch.bfloat16)
+    Z = buf[8:].view(T, V)                      # 16 bytes past a 32-byte boundary
+    Z.copy_(Z0)
+    assert Z.data_ptr() % 32 == 16
+    check(Z, 100)
+
+
+@pytest.mark.parametrize("V,n_eq", [(20000, 2048), (20000, 2049), (20008, 2049),
+                                    (150000, 4096), (150000, 4097), (300000, 4097)])
 def test_candidate_list_capacity(cuda_device, V, n_eq):
     """n_eq equal maxima in one run: every one of them reaches theta, so the
-    candidate list holds exactly n_eq entries.  The narrow shape (a 40 KB row)
-    keeps 2048, the wide shape (a 300 KB row) 4096; one more takes the exact
-    fallback."""
+    candidate list holds exactly n_eq entries.  The narrow shape (40 KB rows,
+    with 32- and with 16-byte loads) keeps 2048, the wide shape (a 300 KB row
+    with 16-byte loads, a 600 KB row with 32-byte loads) 4096; one more takes
+    the exact fallback."""
     Z = make_teacher_logits(3, V, seed=n_eq, device=cuda_device, dtype="bf16")
     top = float(Z.float().max()) + 2.0
     Z[0, 777:777 + n_eq] = top
