@@ -7,17 +7,19 @@
 // here over logits that are already on the device.
 //
 // One block per row (grid-stride over rows): 256-thread blocks, four per SM,
-// for rows of up to 256 KB, 512-thread blocks, two per SM, for longer rows
-// (the block shapes below).  Each row is read from HBM once, with 16-byte
-// loads, several in flight per thread, behind L2 prefetches that keep a
-// window of the row requested ahead of pass 1 (64 KB for the narrow shape,
-// 128 KB for the wide one; the wide shape requests a row of up to 256 KB
-// whole).  The head of the block's next row is requested while the block
-// selects this one, so that HBM keeps streaming through the selection:
+// for rows of up to 512 KB (256 KB when they are read 16 bytes at a time),
+// 512-thread blocks, two per SM, for longer rows (the block shapes below).
+// Each row is read from HBM once, with 32-byte loads (one 256-bit load) when
+// the row is a whole number of 32-byte groups on a 32-byte boundary, 16-byte
+// loads otherwise, several in flight per thread, behind L2 prefetches that
+// keep a window of the row requested ahead of pass 1 (64 KB for the narrow
+// shape, 128 KB for the wide one; the wide shape requests a row of up to
+// 256 KB whole).  The head of the block's next row is requested while the
+// block selects this one, so that HBM keeps streaming through the selection:
 //   pass 1  per-slot maximum (two slots per thread, every element in
 //           exactly one), an online (max, sum of 2^x) for lse, and the maximum
-//           of every 16-byte group, kept in shared memory (as bf16, rounded up
-//           for fp32 logits);
+//           of every load's group (32 or 16 bytes), kept in shared memory (as
+//           bf16, rounded up for fp32 logits);
 //   select  theta = the K-th largest slot maximum, by a byte-wise radix select
 //           over 256-bin shared-memory histograms (with the block's lse
 //           reduced alongside): at least K distinct elements reach theta, so
@@ -53,18 +55,19 @@
 
 namespace kd {
 
-constexpr int CACHE_UNROLL = 4;              // 16-byte loads in flight per thread
+constexpr int CACHE_UNROLL = 4;              // loads in flight per thread, rows read element-wise
 constexpr int CACHE_GLIST = 1024;            // groups listed for the re-read of pass 2
 constexpr int64_t CACHE_WHOLE_ROW = 262144;  // the wide shape prefetches rows up to this many bytes whole
 
-// Block shapes.  Rows of at most 256 KB read 16 bytes at a time, with K at
-// most the narrow shape's slot count, run the narrow shape: 256-thread
-// blocks, four per SM, each row requested into L2 through a 64 KB window
-// (four resident rows per SM requested whole would not fit in L2).  Other
-// rows run the wide shape: 512-thread blocks, two per SM, a row of up to
-// 256 KB requested whole, a longer one through a 128 KB window.  CAP
-// candidates and GMAX 16-byte group maxima are kept in shared memory; HEAD
-// bytes of the block's next row are requested while it selects a row.
+// Block shapes.  The narrow shape (256-thread blocks, four per SM, each row
+// requested into L2 through a 64 KB window, since four resident rows per SM
+// requested whole would not fit in L2) takes rows whose group maxima fit its
+// shared memory: up to 512 KB read 32 bytes at a time, 256 KB read 16 bytes at
+// a time, when K is at most its slot count.  The wide shape (512-thread
+// blocks, two per SM, a row of up to 256 KB requested whole, a longer one
+// through a 128 KB window) takes the rest.  CAP candidates and GMAX group
+// maxima are kept in shared memory; HEAD bytes of the block's next row are
+// requested while it selects a row.
 template <int NT_, int MINB_, int CAP_, int GMAX_, bool ALL_WINDOWED_, int64_t WINDOW_, int64_t HEAD_, int VB_ = 16>
 struct CacheShape {
   static constexpr int NT = NT_;

@@ -691,9 +691,10 @@ kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, in
   const int sms = current_sm_count();
   const int slot = prof_begin(KD_K_OTHER, st);
   cudaError_t e = cudaSuccess;
-  // the narrow block shape for rows of at most 256 KB read 16 bytes at a time,
-  // when its slot maxima can bound the K-th key (K <= its slot count); with
-  // 32-byte loads when every row starts on a 32-byte boundary
+  // 32-byte loads when every row is whole 32-byte groups on a 32-byte boundary;
+  // the narrow block shape when its slot maxima can bound the K-th key (K <=
+  // its slot count) and its group maxima fit (rows of up to 512 KB read 32
+  // bytes at a time, 256 KB read 16 bytes at a time)
   const int64_t row_bytes = int64_t(V) * (logits_bf16 ? 2 : 4);
   const bool v32 = vec && (reinterpret_cast<uintptr_t>(logits) & 31u) == 0 && row_bytes % 32 == 0;
   const bool narrow32 = v32 && row_bytes <= 2 * CACHE_WHOLE_ROW && K <= CacheNarrow32::SLOTS;
