@@ -50,10 +50,10 @@ METRIC = "fused top-K KL fwd+bwd tokens/s & TFLOP/s (fraction of bf16 peak); pea
 # launch per group of two 2048-row chunks, the first group of a step stores dW
 # ("first"), the others reduce-add into it ("rest").  logits_gf: one chunk's G
 # with the next chunk's forward.
-TRAFFIC = {"workload": "longctx", "src_sha": "fe2b7aafccd2f51b", "kinds": {
-    "gemm_dw": {"first": 1370842624 + 1545507072, "rest": 2743538432 + 1534056192},
-    "logits_gf": {"first": 858305792 + 525309952,
-                  "rest": (852527360 + 522702080 + 862584576 + 522403072) // 2},
+TRAFFIC = {"workload": "longctx", "src_sha": "bce7373be8465ed0", "kinds": {
+    "gemm_dw": {"first": 1842127872 + 1546414080, "rest": 3012833536 + 1538813696},
+    "logits_gf": {"first": 971829504 + 525924352,
+                  "rest": (1128472064 + 522564864 + 1067071232 + 522660608) // 2},
 }}
 # sequence lengths of the peak-bytes-versus-T series (the output-head-only benchmark's range)
 PEAK_T = (4096, 8192, 16384, 32768, 65536, 131072, 262144)
