@@ -334,20 +334,21 @@ __device__ __forceinline__ uint16_t gmax_bits(float x) {
   else return __bfloat16_as_ushort(__float2bfloat16_ru(x));
 }
 
-// Statistics of U loaded groups x[0..U): the slot maximum, the online
-// normaliser (m, s), folded group after group, and each group's maximum in
-// gm[u].
+// Statistics of U loaded groups x[0..U): the slot maxima (load u feeds slot
+// u % 2), the online normaliser (m, s), folded group after group, and each
+// group's maximum in gm[u].
 template <int U, typename RV>
 __device__ __forceinline__ void groups_stats(const typename RV::Raw (&x)[U], float (&gm)[U], float& m, float& s,
-                                             float& slot) {
+                                             float& slot0, float& slot1) {
   constexpr int PV = RV::PV;
   float fmx = -INFINITY;
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     gm[u] = RV::gmax(x[u]);
     fmx = fmaxf(fmx, gm[u]);
+    if (u & 1) slot1 = fmaxf(slot1, gm[u]);  // load u of an iteration feeds slot u % 2
+    else slot0 = fmaxf(slot0, gm[u]);
   }
-  slot = fmaxf(slot, fmx);
   if (fmx == -INFINITY) return;  // -inf logits add nothing
   if (fmx > m) {
     s *= ex2((m - fmx) * kLog2e);
@@ -428,9 +429,8 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
     // ---------------- pass 1: slot maxima, online softmax normaliser, group maxima
     float fslot0 = -INFINITY, fslot1 = -INFINITY;  // two disjoint element sets per thread
     float m = -INFINITY, s = 0.f;
-    int it = 0;  // the slot of an iteration alternates
+    int it = 0;
     for (int g0 = tid; g0 < ng; g0 += S::NT * UNR, ++it) {
-      float& slot = (it & 1) ? fslot1 : fslot0;
       // keep the window ahead of what this iteration reads (16 bytes per group)
       if (windowed && tid == 0)
         request_upto(rv.z, static_cast<int64_t>(it + 1) * S::NT * UNR * S::VB + S::WINDOW);
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
         float gm[UNR];
 #pragma unroll
         for (int u = 0; u < UNR; ++u) x[u] = rv.load(g0 + u * S::NT);
-        groups_stats<UNR, RV>(x, gm, m, s, slot);
+        groups_stats<UNR, RV>(x, gm, m, s, fslot0, fslot1);
         if (screen) {
 #pragma unroll
           for (int u = 0; u < UNR; ++u) gmax[g0 + u * S::NT] = gmax_bits<TL>(gm[u]);
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
         for (int u = 0; u < UNR && g0 + u * S::NT < ng; ++u) {
           const typename RV::Raw x[1] = {rv.load(g0 + u * S::NT)};
           float gm[1];
-          groups_stats<1, RV>(x, gm, m, s, slot);
+          groups_stats<1, RV>(x, gm, m, s, fslot0, fslot1);
           if (screen) gmax[g0 + u * S::NT] = gmax_bits<TL>(gm[0]);
         }
       }
@@ -509,21 +509,19 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
       // smallest bf16 >= theta's value
       const __nv_bfloat162 th2 = __bfloat162bfloat162(__float2bfloat16_ru(tv));
       const int nv = (ng + 7) / 8;
-      for (int v0 = warp * 32; v0 < nv; v0 += S::NT) {  // v = tid + k S::NT
-        const int v = v0 + lane;
-        uint32_t m8 = 0;  // bit e: group v * 8 + e reaches theta
-        if (v < nv) {
-          const uint4 w = reinterpret_cast<const uint4*>(gmax)[v];
-          const uint32_t h0 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.x & 0xFFFFu), __ushort_as_bfloat16(w.x >> 16)), th2);
-          const uint32_t h1 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.y & 0xFFFFu), __ushort_as_bfloat16(w.y >> 16)), th2);
-          const uint32_t h2 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.z & 0xFFFFu), __ushort_as_bfloat16(w.z >> 16)), th2);
-          const uint32_t h3 = __hge2_mask(__halves2bfloat162(__ushort_as_bfloat16(w.w & 0xFFFFu), __ushort_as_bfloat16(w.w >> 16)), th2);
-          m8 = (h0 & 1u) | ((h0 >> 15) & 2u) | ((h1 & 1u) << 2) | ((h1 >> 13) & 8u) | ((h2 & 1u) << 4) |
-               ((h2 >> 11) & 32u) | ((h3 & 1u) << 6) | ((h3 >> 9) & 128u);
-          if (v * 8 + 8 > ng) m8 &= (1u << (ng - v * 8)) - 1u;  // groups past the row's end
-        }
-        if (!__any_sync(0xffffffffu, m8 != 0)) continue;  // the common case
-        int at = warp_reserve(&s_groups, __popc(m8));
+      for (int v = tid; v < nv; v += S::NT) {
+        const uint4 w = reinterpret_cast<const uint4*>(gmax)[v];
+        // the common case first: none of the eight maxima reaches theta (entries
+        // past the row's end may hold anything; the exact mask below drops them)
+        const __nv_bfloat162* h8 = reinterpret_cast<const __nv_bfloat162*>(&w);
+        if (!__hge2_mask(__hmax2(__hmax2(h8[0], h8[1]), __hmax2(h8[2], h8[3])), th2)) continue;
+        const uint32_t h0 = __hge2_mask(h8[0], th2), h1 = __hge2_mask(h8[1], th2);
+        const uint32_t h2 = __hge2_mask(h8[2], th2), h3 = __hge2_mask(h8[3], th2);
+        uint32_t m8 = (h0 & 1u) | ((h0 >> 15) & 2u) | ((h1 & 1u) << 2) | ((h1 >> 13) & 8u) | ((h2 & 1u) << 4) |
+                      ((h2 >> 11) & 32u) | ((h3 & 1u) << 6) | ((h3 >> 9) & 128u);  // bit e: group v * 8 + e
+        if (v * 8 + 8 > ng) m8 &= (1u << (ng - v * 8)) - 1u;  // groups past the row's end
+        if (!m8) continue;
+        int at = atomicAdd(&s_groups, __popc(m8));  // one shared atomic per lane with hits
         for (; m8; m8 &= m8 - 1u, ++at) {
           const int g = v * 8 + __ffs(m8) - 1;
           if (at < CACHE_GLIST) {
@@ -532,8 +530,8 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
             float f[PV];
             RV::floats(rv.load(g), f);
 #pragma unroll
-            for (int i = 0; i < PV; ++i)
-              if (f[i] >= tv) push_cand<S::CAP>(cand, &s_count, Tr::fkey(f[i]), g * PV + i);
+            for (int e = 0; e < PV; ++e)
+              if (f[e] >= tv) push_cand<S::CAP>(cand, &s_count, Tr::fkey(f[e]), g * PV + e);
           }
         }
       }
