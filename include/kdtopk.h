@@ -211,8 +211,9 @@ KD_API kd_status kd_topk_kl_forward_noalloc(const void* H, const void* W, const 
  * probability; NaN logits are not supported (their rank and the row's p and
  * lse are unspecified).  1 <= K <= min(V, 1024) (KD_ERR_INVALID_ARG /
  * KD_ERR_UNSUPPORTED otherwise).  Rows whose length in bytes is a multiple
- * of 16 (with a 16-byte aligned base) are read with 16-byte loads, others
- * element by element.  Allocates nothing, waits on nothing (no device-side
+ * of 32 (with a 32-byte aligned base) are read with 32-byte loads, those
+ * whose length is a multiple of 16 (16-byte aligned base) with 16-byte loads,
+ * others element by element; the results are the same either way.  Allocates nothing, waits on nothing (no device-side
  * errors are possible); asynchronous on `stream`.
  */
 KD_API kd_status kd_topk_cache_build(const void* logits, int logits_bf16, int64_t T, int V, int K,
