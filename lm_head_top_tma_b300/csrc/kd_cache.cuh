@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
   // thread 0: bytes of the current row already requested into L2, and of the
   // block's next row (its head, requested during this row's selection)
   int64_t req = 0, req_next = 0;
-  auto request_upto = [&](const TL* rz, int64_t upto) {  // 16-byte multiples, within the row
+  auto request_upto = [&](const TL* rz, int64_t upto) {  // multiples of 16 bytes, within the row
     upto = min(upto, row_bytes);
     if (upto > req) {
       prefetch_l2_bulk(reinterpret_cast<const char*>(rz) + req, upto - req);
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
     float m = -INFINITY, s = 0.f;
     int it = 0;
     for (int g0 = tid; g0 < ng; g0 += S::NT * UNR, ++it) {
-      // keep the window ahead of what this iteration reads (16 bytes per group)
+      // keep the window ahead of what this iteration reads (VB bytes per group)
       if (windowed && tid == 0)
         request_upto(rv.z, static_cast<int64_t>(it + 1) * S::NT * UNR * S::VB + S::WINDOW);
       if (g0 + (UNR - 1) * S::NT < ng) {
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(S::NT, S::MINB)
         }
       }
     }
-    // (rows read 16 bytes at a time are whole groups: there is no tail)
+    // (rows read in vectors are whole groups: there is no tail)
     // slots without elements hold -inf: no larger than any element, so they never raise theta
     const uint32_t kslot0 = Tr::fkey(fslot0), kslot1 = Tr::fkey(fslot1);
 #pragma unroll
