@@ -81,6 +81,28 @@ def test_host_argument_checks(lib):
                                   fake, fake, null, fake, 1 << 30, null) == N.KD_ERR_UNSUPPORTED
 
 
+def test_cache_builder_argument_checks(lib):
+    """kd_topk_cache_build rejects bad arguments before it touches the device:
+    null pointers and sizes outside 1 <= K <= V (invalid), K above 1024 and
+    logits or outputs not aligned to their element type (unsupported)."""
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: checks fail first
+    build_cache = lib.kd_topk_cache_build
+    assert build_cache(null, 1, 8, 4096, 100, fake, fake, null, null) == N.KD_ERR_INVALID_ARG
+    assert build_cache(fake, 1, 8, 4096, 100, null, fake, null, null) == N.KD_ERR_INVALID_ARG
+    assert build_cache(fake, 1, 8, 4096, 100, fake, null, null, null) == N.KD_ERR_INVALID_ARG
+    assert build_cache(fake, 1, 0, 4096, 100, fake, fake, null, null) == N.KD_ERR_INVALID_ARG
+    assert build_cache(fake, 1, 8, 64, 65, fake, fake, null, null) == N.KD_ERR_INVALID_ARG
+    assert build_cache(fake, 1, 8, 4096, 0, fake, fake, null, null) == N.KD_ERR_INVALID_ARG
+    assert build_cache(fake, 1, 8, 4096, 1025, fake, fake, null, null) == N.KD_ERR_UNSUPPORTED
+    odd = ctypes.c_void_p((1 << 20) + 1)
+    two = ctypes.c_void_p((1 << 20) + 2)
+    assert build_cache(odd, 1, 8, 4096, 100, fake, fake, null, null) == N.KD_ERR_UNSUPPORTED   # bf16
+    assert build_cache(two, 0, 8, 4096, 100, fake, fake, null, null) == N.KD_ERR_UNSUPPORTED   # fp32
+    assert build_cache(fake, 1, 8, 4096, 100, two, fake, null, null) == N.KD_ERR_UNSUPPORTED
+    assert build_cache(fake, 1, 8, 4096, 100, fake, fake, two, null) == N.KD_ERR_UNSUPPORTED
+
+
 def test_workspace_is_flat_in_T(lib):
     f = lambda T, what=N.KD_WS_FUSED: lib.kd_topk_kl_workspace_size(T, 3072, 128256, 100, 2048, what)
     # flat once T covers one dW group (two 2048-row chunks here); a single chunk needs less
@@ -102,3 +124,17 @@ def test_missing_library_fails_loudly(tmp_path):
     """No fallback: a library that is not there is an error, not a slower path."""
     with pytest.raises(RuntimeError, match="not found"):
         N.load(str(tmp_path / "libkdtopk.so"))
+
+
+def test_grad_to_bf16_argument_checks(lib):
+    """kd_grad_to_bf16: null pointers and negative lengths are invalid, an empty
+    range is a no-op, and a source off a 16-byte boundary or a destination off
+    an 8-byte boundary is unsupported, all before any device work."""
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.kd_grad_to_bf16(null, fake, 16, 1.0, null) == N.KD_ERR_INVALID_ARG
+    assert lib.kd_grad_to_bf16(fake, null, 16, 1.0, null) == N.KD_ERR_INVALID_ARG
+    assert lib.kd_grad_to_bf16(fake, fake, -1, 1.0, null) == N.KD_ERR_INVALID_ARG
+    assert lib.kd_grad_to_bf16(fake, fake, 0, 1.0, null) == N.KD_OK
+    assert lib.kd_grad_to_bf16(ctypes.c_void_p((1 << 20) + 4), fake, 16, 1.0, null) == N.KD_ERR_UNSUPPORTED
+    assert lib.kd_grad_to_bf16(fake, ctypes.c_void_p((1 << 20) + 4), 16, 1.0, null) == N.KD_ERR_UNSUPPORTED
