@@ -12,8 +12,8 @@
 // Each row is read from HBM once, with 32-byte loads (one 256-bit load) when
 // the row is a whole number of 32-byte groups on a 32-byte boundary, 16-byte
 // loads otherwise, several in flight per thread, behind L2 prefetches that
-// keep a window of the row requested ahead of pass 1 (64 KB for the narrow
-// shape, 128 KB for the wide one; the wide shape requests a row of up to
+// keep a window of the row requested ahead of pass 1 (48 KB for the narrow
+// shape with 32-byte loads, 64 KB with 16-byte loads, 128 KB for the wide one; the wide shape requests a row of up to
 // 256 KB whole).  The head of the block's next row is requested while the
 // block selects this one, so that HBM keeps streaming through the selection:
 //   pass 1  per-slot maximum (two slots per thread, every element in
@@ -60,7 +60,7 @@ constexpr int CACHE_GLIST = 1024;            // groups listed for the re-read of
 constexpr int64_t CACHE_WHOLE_ROW = 262144;  // the wide shape prefetches rows up to this many bytes whole
 
 // Block shapes.  The narrow shape (256-thread blocks, four per SM, each row
-// requested into L2 through a 64 KB window, since four resident rows per SM
+// requested into L2 through a 48 or 64 KB window, since four resident rows per SM
 // requested whole would not fit in L2) takes rows whose group maxima fit its
 // shared memory: up to 512 KB read 32 bytes at a time, 256 KB read 16 bytes at
 // a time, when K is at most its slot count.  The wide shape (512-thread
@@ -87,7 +87,7 @@ struct CacheShape {
   static constexpr int smem_bytes(bool vec) { return CAP * 8 + (vec ? GMAX * 2 : 0); }
 };
 using CacheNarrow = CacheShape<256, 4, 2048, 16384, true, 65536, 32768>;
-using CacheNarrow32 = CacheShape<256, 4, 2048, 16384, true, 65536, 32768, 32>;
+using CacheNarrow32 = CacheShape<256, 4, 2048, 16384, true, 49152, 16384, 32>;
 using CacheWide = CacheShape<512, 2, 4096, 32768, false, 131072, 65536>;
 using CacheWide32 = CacheShape<512, 2, 4096, 32768, false, 131072, 65536, 32>;
 
